@@ -1,0 +1,178 @@
+/*
+ * pagedattn -- paged grouped-query decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Every pointer argument named "device" is CUDA device memory of the
+ * pool's device; sizes are element counts unless stated; no call throws.
+ * Device work is enqueued on `stream` (a cudaStream_t passed as void*, NULL
+ * for the legacy default stream) and is asynchronous: no call synchronises
+ * except pa_get_device_error.
+ *
+ * The operation (sources named by page title and section):
+ *  - Paged KV cache: K/V live in fixed-size physical blocks; a per-sequence
+ *    block table maps logical block i to a physical block, and token t of a
+ *    sequence sits in slot t % block_size of block block_table[t / block_size]
+ *    ("十年 C++ 后端 GAP 六个月 ... TFFInfer", section 3.6.4 KVCache:
+ *    PageManager, LayerKVContext::get_location; heterogeneous C++ LLM engine
+ *    article, sections 2.3 and 4.3).
+ *  - KV quantisation: asymmetric per-channel codes, scale = (max-min)/L,
+ *    zero_point = round(-min/scale), Q = clamp(round(x/scale)+zp, 0, L),
+ *    dequantised as (Q - zp) * scale, with L = 255 (uint8) or 15 (uint4, two
+ *    codes per byte) (engine article, sections 2.4, 2.6, 4.4).
+ *  - Decode attention: for each sequence b and query head h, with KV head
+ *    j = h / (Hq / Hkv) (GQA as in "从零实现 C++ LLM 推理引擎", section
+ *    "3. GQA"), out = softmax(q . K^T * softmax_scale) . V over the
+ *    sequence's seq_len cached tokens (engine article, section 4.3
+ *    paged_attention_kernel; online softmax of the TFFInfer article, section
+ *    3.7.2 item 5).
+ *
+ * Storage format of a pool (library-owned device memory, one allocation):
+ *   bf16 : K, V     bf16  [num_blocks][Hkv][block_size][head_dim]
+ *   uint8: K, V     uint8 [num_blocks][Hkv][block_size][head_dim]
+ *   uint4: K, V     uint8 [num_blocks][Hkv][block_size][head_dim/2],
+ *                   channel 2i in the low nibble, 2i+1 in the high nibble
+ *   quantised pools also hold, for K and for V, scale float32 and zero point
+ *   int32 [num_blocks][Hkv][head_dim] -- one pair per (physical block, kv
+ *   head, channel). Every page (one block of one kv head) starts on a 256-byte
+ *   boundary.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_UINT8 = 1, PA_KV_UINT4 = 2 } pa_kv_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size or count; nothing launched */
+  PA_ERR_UNSUPPORTED = 2,   /* head_dim/block_size/group size/dtype not built */
+  PA_ERR_OOM = 3,           /* device allocation failed, or workspace too small */
+  PA_ERR_CUDA = 4,          /* a CUDA runtime call failed (see pa_last_error) */
+  PA_ERR_DEVICE_BOUNDS = 5, /* pa_get_device_error: a kernel met a bad index */
+  PA_ERR_TIMEOUT = 6        /* pa_get_device_error: a kernel wait gave up */
+} pa_status;
+
+/* Bits of the per-pool device error word (pa_get_device_error). Kernels set
+ * them with atomicOr and skip the offending work; they never trap. */
+#define PA_DEVERR_BLOCK_TABLE 0x1u /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 0x2u     /* length < 0 or > max_blocks * block_size */
+#define PA_DEVERR_APPEND 0x4u      /* cu_new not non-decreasing */
+#define PA_DEVERR_TIMEOUT 0x8u     /* a bounded mbarrier wait expired */
+
+typedef struct pa_pool pa_pool; /* opaque, library-owned */
+
+typedef struct {
+  int32_t num_blocks;   /* physical blocks, >= 1 */
+  int32_t block_size;   /* tokens per block: 16 or 32 */
+  int32_t num_kv_heads; /* >= 1 */
+  int32_t head_dim;     /* 64 or 128 */
+  int32_t kv_dtype;     /* pa_kv_dtype */
+  int32_t device;       /* CUDA device ordinal */
+} pa_pool_desc;
+
+/* Device addresses of a pool's arrays (layouts above). Scale and zero-point
+ * pointers are NULL for a bf16 pool. */
+typedef struct {
+  void* k;
+  void* v;
+  float* k_scale;
+  int32_t* k_zp;
+  float* v_scale;
+  int32_t* v_zp;
+  size_t kv_bytes;   /* bytes of each of k and v */
+  size_t meta_bytes; /* bytes of each scale / zero-point array (0 for bf16) */
+} pa_pool_buffers;
+
+/* pa_create_pool: allocate a pool (one device allocation; contents zero,
+ * scales 1.0) on desc->device and return its handle in *out.
+ * Errors: PA_ERR_INVALID_ARG (null pointer, counts < 1), PA_ERR_UNSUPPORTED
+ * (block_size not 16/32, head_dim not 64/128, unknown dtype), PA_ERR_OOM.
+ * The pool owns its memory until pa_destroy. */
+PA_API pa_status pa_create_pool(const pa_pool_desc* desc, pa_pool** out);
+
+/* pa_destroy: free the pool (synchronises the device first). NULL is a no-op. */
+PA_API pa_status pa_destroy(pa_pool* pool);
+
+/* pa_append_kv: store new tokens' K and V into their blocks (engine article
+ * section 2.6 formula for quantised pools; TFFInfer section 3.6.4 addressing).
+ *   k_new, v_new   device bf16 [T_new][Hkv][head_dim]; sequence b's new tokens
+ *                  are rows cu_new[b] .. cu_new[b+1]-1
+ *   cu_new         device int32 [batch+1], non-decreasing, cu_new[0] = 0
+ *   ctx_lens       device int32 [batch]: tokens already stored for b; the new
+ *                  tokens take logical positions ctx_lens[b], ctx_lens[b]+1, ...
+ *   block_table    device int32 [batch][max_blocks] (row stride max_blocks)
+ *   max_new_per_seq upper bound on cu_new[b+1]-cu_new[b] (sizes the grid;
+ *                  0 = unknown, taken as max_blocks*block_size)
+ * bf16 pools get an exact copy of the bits. Quantised pools re-quantise every
+ * touched (block, kv head, channel) over the block's valid tokens: stored
+ * tokens enter as float(code - zp) * scale, new ones as their bf16 value;
+ * scale = (max-min)/L (or |min|/L, or 1.0, for an empty range),
+ * zp = rint(-min/scale) (int32, unclamped), code = clamp(rint(x/scale)+zp, 0, L),
+ * all in IEEE fp32. A block written by one sequence must not be written by
+ * another sequence in the same call. Bad table entries or lengths set the
+ * device error word and skip that block or sequence. */
+PA_API pa_status pa_append_kv(pa_pool* pool, const void* k_new, const void* v_new, const int32_t* cu_new,
+                       const int32_t* ctx_lens, const int32_t* block_table, int32_t batch,
+                       int32_t max_blocks, int32_t max_new_per_seq, void* stream);
+
+/* pa_decode: one decode step of grouped-query attention over the paged pool
+ * (engine article section 4.3; TFFInfer section 3.7.2 online softmax).
+ *   q            device bf16 [batch][num_q_heads][head_dim]
+ *   block_table  device int32 [batch][max_blocks]
+ *   seq_lens     device int32 [batch]: tokens to attend (the step's new token
+ *                already appended); 0 gives a zero output row
+ *   softmax_scale usually 1/sqrt(head_dim)
+ *   out          device float32 [batch][num_q_heads][head_dim]
+ *   workspace    device scratch of at least pa_decode_workspace_bytes(...)
+ *                bytes (256-byte aligned), caller-owned; not read before written
+ *   num_splits   number of equal partitions of the (sequence, kv head, block)
+ *                work list, one thread block each (0 = one per resident slot
+ *                of the device). Sequences cut by a partition boundary are
+ *                merged by a log-sum-exp combine kernel.
+ * num_q_heads must be a multiple of Hkv with a group size Hq/Hkv <= 8.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OOM (workspace too
+ * small), PA_ERR_CUDA. Bad table entries or lengths set the device error
+ * word; the affected blocks are skipped. */
+PA_API pa_status pa_decode(pa_pool* pool, const void* q, const int32_t* block_table,
+                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                    int32_t max_blocks, float softmax_scale, float* out, void* workspace,
+                    size_t workspace_bytes, int32_t num_splits, void* stream);
+
+/* Bytes of workspace pa_decode needs for this batch, head count and split
+ * count (0 = the automatic split count); 0 on invalid arguments. */
+PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_splits);
+
+/* Resolve num_splits = 0 to the partition count pa_decode would use. */
+PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
+
+/* Device addresses of the pool's arrays, for inspection and tests. */
+PA_API pa_status pa_pool_view(const pa_pool* pool, pa_pool_buffers* out);
+
+/* Synchronise `stream`, return the pool's device error bits in *flags and
+ * clear them. Returns PA_ERR_DEVICE_BOUNDS / PA_ERR_TIMEOUT when bits were
+ * set, PA_ERR_CUDA if the synchronisation failed, else PA_OK. */
+PA_API pa_status pa_get_device_error(pa_pool* pool, void* stream, uint32_t* flags);
+
+/* Static description of a status code. */
+PA_API const char* pa_status_string(pa_status s);
+
+/* Message of the last failed call on this thread ("" if none). */
+PA_API const char* pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

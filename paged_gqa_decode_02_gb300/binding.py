@@ -1,0 +1,227 @@
+"""Thin ctypes binding of libpagedattn (include/pagedattn.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. torch supplies device memory and streams. The functions keep the C
+names (pa_create_pool, pa_append_kv, pa_decode, pa_destroy, ...); PagedKVPool
+is a small convenience wrapper over them.
+
+If the shared library is missing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "pagedattn.h")
+
+PA_KV_BF16, PA_KV_UINT8, PA_KV_UINT4 = 0, 1, 2
+KV_DTYPES = {"bf16": PA_KV_BF16, "uint8": PA_KV_UINT8, "uint4": PA_KV_UINT4}
+STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
+          4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE_BOUNDS", 6: "PA_ERR_TIMEOUT"}
+DEVERR_BLOCK_TABLE, DEVERR_SEQ_LEN, DEVERR_APPEND, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class pa_pool_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("device", ctypes.c_int32)]
+
+
+class pa_pool_buffers(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("k_zp", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("v_zp", ctypes.c_void_p),
+                ("kv_bytes", ctypes.c_size_t), ("meta_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def header_symbols():
+    """Function names declared in include/pagedattn.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:PA_API\s+)?(?:pa_status|size_t|int32_t|const char\*)\s+(pa_\w+)\s*\(",
+                                 text, re.M)))
+
+
+def lib():
+    """Load libpagedattn.so (built by paged_gqa_decode_02_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run paged_gqa_decode_02_gb300.build.build() "
+                               "(the CUDA library is required; there is no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.pa_create_pool.argtypes = [ctypes.POINTER(pa_pool_desc), ctypes.POINTER(P)]
+        L.pa_destroy.argtypes = [P]
+        L.pa_append_kv.argtypes = [P, P, P, P, P, P, I32, I32, I32, P]
+        L.pa_decode.argtypes = [P, P, P, P, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
+        L.pa_decode_workspace_bytes.argtypes = [P, I32, I32, I32]
+        L.pa_decode_workspace_bytes.restype = SZ
+        L.pa_decode_num_splits.argtypes = [P, I32]
+        L.pa_decode_num_splits.restype = I32
+        L.pa_pool_view.argtypes = [P, ctypes.POINTER(pa_pool_buffers)]
+        L.pa_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+        L.pa_status_string.argtypes = [I32]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_last_error.argtypes = []
+        L.pa_last_error.restype = ctypes.c_char_p
+        for f in ("pa_create_pool", "pa_destroy", "pa_append_kv", "pa_decode", "pa_pool_view",
+                  "pa_get_device_error"):
+            getattr(L, f).restype = I32
+        _lib = L
+        return L
+
+
+def _check(status):
+    if status != 0:
+        raise PagedAttnError(status, lib().pa_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ------------------------------------------------------------------ C-named entry points
+def pa_create_pool(num_blocks, block_size, num_kv_heads, head_dim, kv_dtype, device=0):
+    d = pa_pool_desc(int(num_blocks), int(block_size), int(num_kv_heads), int(head_dim),
+                     KV_DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype), int(device))
+    h = ctypes.c_void_p()
+    _check(lib().pa_create_pool(ctypes.byref(d), ctypes.byref(h)))
+    return h
+
+
+def pa_destroy(handle):
+    _check(lib().pa_destroy(handle))
+
+
+def pa_append_kv(handle, k_new, v_new, cu_new, ctx_lens, block_table, batch, max_blocks,
+                 max_new_per_seq=0, stream=None):
+    _check(lib().pa_append_kv(handle, _ptr(k_new), _ptr(v_new), _ptr(cu_new), _ptr(ctx_lens),
+                              _ptr(block_table), int(batch), int(max_blocks), int(max_new_per_seq),
+                              _stream(stream)))
+
+
+def pa_decode(handle, q, block_table, seq_lens, batch, num_q_heads, max_blocks, softmax_scale, out,
+              workspace, workspace_bytes, num_splits=0, stream=None):
+    _check(lib().pa_decode(handle, _ptr(q), _ptr(block_table), _ptr(seq_lens), int(batch),
+                           int(num_q_heads), int(max_blocks), float(softmax_scale), _ptr(out),
+                           _ptr(workspace), int(workspace_bytes), int(num_splits), _stream(stream)))
+
+
+def pa_decode_workspace_bytes(handle, batch, num_q_heads, num_splits=0):
+    return int(lib().pa_decode_workspace_bytes(handle, int(batch), int(num_q_heads), int(num_splits)))
+
+
+def pa_decode_num_splits(handle, num_splits=0):
+    return int(lib().pa_decode_num_splits(handle, int(num_splits)))
+
+
+def pa_get_device_error(handle, stream=None):
+    flags = ctypes.c_uint32(0)
+    st = lib().pa_get_device_error(handle, _stream(stream), ctypes.byref(flags))
+    return st, int(flags.value)
+
+
+class _DevArray:
+    """Exposes a device address range to torch via __cuda_array_interface__."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 2, "strides": None}
+
+
+def _view(ptr, shape, typestr, device):
+    return torch.as_tensor(_DevArray(ptr, shape, typestr), device=device)
+
+
+class PagedKVPool:
+    """A paged KV pool on one GPU (owns a pa_pool handle)."""
+
+    def __init__(self, num_blocks, block_size, num_kv_heads, head_dim, kv_dtype="bf16", device=0):
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.num_kv_heads, self.head_dim = int(num_kv_heads), int(head_dim)
+        self.kv_dtype = kv_dtype
+        self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        with torch.cuda.device(self.device):
+            self.handle = pa_create_pool(num_blocks, block_size, num_kv_heads, head_dim, kv_dtype,
+                                         self.device.index)
+        self._ws = None
+
+    def close(self):
+        if self.handle is not None:
+            pa_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def view(self):
+        """torch tensors aliasing the pool's device arrays (see pagedattn.h)."""
+        b = pa_pool_buffers()
+        _check(lib().pa_pool_view(self.handle, ctypes.byref(b)))
+        P, H, bs, D = self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim
+        dev = self.device
+        if self.kv_dtype == "bf16":
+            return {"k": _view(b.k, (P, H, bs, D), "<i2", dev), "v": _view(b.v, (P, H, bs, D), "<i2", dev)}
+        w = D if self.kv_dtype == "uint8" else D // 2
+        return {"k": _view(b.k, (P, H, bs, w), "|u1", dev), "v": _view(b.v, (P, H, bs, w), "|u1", dev),
+                "k_scale": _view(b.k_scale, (P, H, D), "<f4", dev),
+                "k_zp": _view(b.k_zp, (P, H, D), "<i4", dev),
+                "v_scale": _view(b.v_scale, (P, H, D), "<f4", dev),
+                "v_zp": _view(b.v_zp, (P, H, D), "<i4", dev)}
+
+    def append_kv(self, k_new, v_new, cu_new, ctx_lens, block_table, max_new_per_seq=0, stream=None):
+        B = int(ctx_lens.shape[0])
+        pa_append_kv(self.handle, k_new, v_new, cu_new, ctx_lens, block_table, B,
+                     int(block_table.shape[1]) if B else 0, max_new_per_seq, stream)
+
+    def workspace_bytes(self, batch, num_q_heads, num_splits=0):
+        return pa_decode_workspace_bytes(self.handle, batch, num_q_heads, num_splits)
+
+    def num_splits(self, num_splits=0):
+        return pa_decode_num_splits(self.handle, num_splits)
+
+    def workspace(self, batch, num_q_heads, num_splits=0):
+        n = self.workspace_bytes(batch, num_q_heads, num_splits)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def decode(self, q, block_table, seq_lens, softmax_scale, out=None, workspace=None, num_splits=0,
+               stream=None):
+        B, Hq, D = q.shape
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device=self.device)
+        if workspace is None:
+            workspace = self.workspace(B, Hq, num_splits)
+        pa_decode(self.handle, q, block_table, seq_lens, B, Hq, int(block_table.shape[1]),
+                  softmax_scale, out, workspace, workspace.numel(), num_splits, stream)
+        return out
+
+    def device_error(self, stream=None):
+        return pa_get_device_error(self.handle, stream)

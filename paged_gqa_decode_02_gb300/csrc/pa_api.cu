@@ -1,0 +1,276 @@
+// C ABI of libpagedattn: pool lifetime, argument validation, dispatch.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+#include "pagedattn.h"
+
+struct pa_pool {
+  pa_pool_desc desc;
+  void* slab;
+  size_t slab_bytes;
+  pa::PoolDev dev;
+  size_t kv_bytes;
+  size_t meta_bytes;
+  int sm_count;
+};
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+pa_status fail(pa_status s, const char* fmt, const char* detail = "") {
+  snprintf(g_last_error, sizeof g_last_error, fmt, detail);
+  return s;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
+  return PA_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+__global__ void fill_f32(float* p, size_t n, float v) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sets the pool's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) err = cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+int auto_splits(const pa_pool* p, int group) {
+  return p->sm_count * pa::decode_ctas_per_sm(p->desc.kv_dtype, p->desc.block_size,
+                                              p->desc.head_dim, group);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_OOM: return "out of device memory or workspace too small";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_DEVICE_BOUNDS: return "device-side bounds violation";
+    case PA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* pa_last_error(void) { return g_last_error; }
+
+pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
+  g_last_error[0] = 0;
+  if (!d || !out) return fail(PA_ERR_INVALID_ARG, "null descriptor or output pointer%s");
+  *out = nullptr;
+  if (d->num_blocks < 1 || d->num_kv_heads < 1 || d->device < 0)
+    return fail(PA_ERR_INVALID_ARG, "num_blocks, num_kv_heads must be >= 1 and device >= 0%s");
+  if (d->block_size != 16 && d->block_size != 32)
+    return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32%s");
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128%s");
+  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_UINT8 && d->kv_dtype != PA_KV_UINT4)
+    return fail(PA_ERR_UNSUPPORTED, "unknown kv_dtype%s");
+  DeviceGuard dg(d->device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  const size_t pages = (size_t)d->num_blocks * d->num_kv_heads;
+  const size_t elem_bits = d->kv_dtype == PA_KV_BF16 ? 16 : (d->kv_dtype == PA_KV_UINT8 ? 8 : 4);
+  const size_t page_bytes = (size_t)d->block_size * d->head_dim * elem_bits / 8;
+  const size_t kv_bytes = pages * page_bytes;
+  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : pages * d->head_dim * 4;
+  const size_t slab = 256 + 2 * align256(kv_bytes) + 4 * align256(meta_bytes);
+  pa_pool* p = new (std::nothrow) pa_pool();
+  if (!p) return fail(PA_ERR_OOM, "host allocation failed%s");
+  p->desc = *d;
+  p->kv_bytes = kv_bytes;
+  p->meta_bytes = meta_bytes;
+  cudaError_t e = cudaMalloc(&p->slab, slab);
+  if (e != cudaSuccess) {
+    delete p;
+    cudaGetLastError();
+    return fail(PA_ERR_OOM, "cudaMalloc of the pool failed%s");
+  }
+  p->slab_bytes = slab;
+  uint8_t* base = static_cast<uint8_t*>(p->slab);
+  p->dev.err = reinterpret_cast<uint32_t*>(base);
+  uint8_t* cur = base + 256;
+  p->dev.k = cur;
+  cur += align256(kv_bytes);
+  p->dev.v = cur;
+  cur += align256(kv_bytes);
+  p->dev.k_scale = nullptr;
+  p->dev.k_zp = nullptr;
+  p->dev.v_scale = nullptr;
+  p->dev.v_zp = nullptr;
+  if (meta_bytes) {
+    p->dev.k_scale = reinterpret_cast<float*>(cur);
+    cur += align256(meta_bytes);
+    p->dev.k_zp = reinterpret_cast<int32_t*>(cur);
+    cur += align256(meta_bytes);
+    p->dev.v_scale = reinterpret_cast<float*>(cur);
+    cur += align256(meta_bytes);
+    p->dev.v_zp = reinterpret_cast<int32_t*>(cur);
+  }
+  p->dev.num_blocks = d->num_blocks;
+  p->dev.num_kv_heads = d->num_kv_heads;
+  p->dev.block_size = d->block_size;
+  p->dev.head_dim = d->head_dim;
+  e = cudaMemset(p->slab, 0, slab);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, d->device);
+  if (e == cudaSuccess && meta_bytes) {
+    // scales start at 1.0 so an untouched page dequantises to its (zero) codes
+    const size_t n = meta_bytes / 4;
+    fill_f32<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256>>>(p->dev.k_scale, n, 1.0f);
+    fill_f32<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256>>>(p->dev.v_scale, n, 1.0f);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
+  if (e != cudaSuccess) {
+    cudaFree(p->slab);
+    delete p;
+    return cuda_fail(e, "pool initialisation");
+  }
+  *out = p;
+  return PA_OK;
+}
+
+pa_status pa_destroy(pa_pool* p) {
+  g_last_error[0] = 0;
+  if (!p) return PA_OK;
+  DeviceGuard dg(p->desc.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t e2 = cudaFree(p->slab);
+  delete p;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
+  return PA_OK;
+}
+
+pa_status pa_pool_view(const pa_pool* p, pa_pool_buffers* out) {
+  if (!p || !out) return fail(PA_ERR_INVALID_ARG, "null pool or output%s");
+  out->k = p->dev.k;
+  out->v = p->dev.v;
+  out->k_scale = p->dev.k_scale;
+  out->k_zp = p->dev.k_zp;
+  out->v_scale = p->dev.v_scale;
+  out->v_zp = p->dev.v_zp;
+  out->kv_bytes = p->kv_bytes;
+  out->meta_bytes = p->meta_bytes;
+  return PA_OK;
+}
+
+pa_status pa_get_device_error(pa_pool* p, void* stream, uint32_t* flags) {
+  g_last_error[0] = 0;
+  if (!p || !flags) return fail(PA_ERR_INVALID_ARG, "null pool or flags%s");
+  DeviceGuard dg(p->desc.device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, p->dev.err, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->dev.err, 0, sizeof host, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *flags = host;
+  if (host & PA_DEVERR_TIMEOUT) return fail(PA_ERR_TIMEOUT, "a kernel wait timed out%s");
+  if (host) return fail(PA_ERR_DEVICE_BOUNDS, "a kernel met a bad table entry or length%s");
+  return PA_OK;
+}
+
+pa_status pa_append_kv(pa_pool* p, const void* k_new, const void* v_new, const int32_t* cu_new,
+                       const int32_t* ctx_lens, const int32_t* block_table, int32_t batch,
+                       int32_t max_blocks, int32_t max_new_per_seq, void* stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  if (batch < 0 || max_blocks < 0 || max_new_per_seq < 0)
+    return fail(PA_ERR_INVALID_ARG, "negative batch, max_blocks or max_new_per_seq%s");
+  if (batch == 0) return PA_OK;
+  if (!k_new || !v_new || !cu_new || !ctx_lens || !block_table || max_blocks == 0)
+    return fail(PA_ERR_INVALID_ARG, "null device pointer or max_blocks == 0%s");
+  DeviceGuard dg(p->desc.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  const int bs = p->desc.block_size;
+  long long max_new = max_new_per_seq > 0 ? max_new_per_seq : (long long)max_blocks * bs;
+  long long touched = (max_new + bs - 1) / bs + 1;
+  if (touched > max_blocks) touched = max_blocks;
+  if (touched < 1) touched = 1;
+  if (touched > 65535) touched = 65535;
+  cudaError_t e = pa::launch_append(p->desc.kv_dtype, p->dev, k_new, v_new, cu_new, ctx_lens,
+                                    block_table, batch, max_blocks, (int)touched,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_quant_append launch");
+  return PA_OK;
+}
+
+int32_t pa_decode_num_splits(const pa_pool* p, int32_t num_splits) {
+  if (!p || num_splits < 0) return 0;
+  return num_splits > 0 ? num_splits : auto_splits(p, 8);
+}
+
+size_t pa_decode_workspace_bytes(const pa_pool* p, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_splits) {
+  if (!p || batch < 0 || num_q_heads < 1 || num_splits < 0) return 0;
+  const int Hkv = p->desc.num_kv_heads;
+  if (num_q_heads % Hkv) return 0;
+  const int group = num_q_heads / Hkv;
+  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, group);
+  return pa::decode_workspace_bytes(ctas, batch, Hkv, group, p->desc.head_dim);
+}
+
+pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
+                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                    int32_t max_blocks, float softmax_scale, float* out, void* workspace,
+                    size_t workspace_bytes, int32_t num_splits, void* stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  if (batch < 0 || max_blocks < 0 || num_splits < 0)
+    return fail(PA_ERR_INVALID_ARG, "negative batch, max_blocks or num_splits%s");
+  if (num_q_heads < 1 || num_q_heads % p->desc.num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads%s");
+  const int group = num_q_heads / p->desc.num_kv_heads;
+  if (group > 8) return fail(PA_ERR_UNSUPPORTED, "GQA group size above 8%s");
+  if (!isfinite(softmax_scale)) return fail(PA_ERR_INVALID_ARG, "softmax_scale is not finite%s");
+  if (batch == 0) return PA_OK;
+  if (!q || !block_table || !seq_lens || !out || !workspace || max_blocks == 0)
+    return fail(PA_ERR_INVALID_ARG, "null device pointer or max_blocks == 0%s");
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(PA_ERR_INVALID_ARG, "q must be 16-byte aligned and workspace 256-byte aligned%s");
+  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, group);
+  const size_t need = pa::decode_workspace_bytes(ctas, batch, p->desc.num_kv_heads, group,
+                                                 p->desc.head_dim);
+  if (workspace_bytes < need) return fail(PA_ERR_OOM, "workspace smaller than pa_decode_workspace_bytes()%s");
+  DeviceGuard dg(p->desc.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  pa::DecodeLaunch L = {};
+  L.num_ctas = ctas;
+  L.group = group;
+  L.num_q_heads = num_q_heads;
+  L.batch = batch;
+  L.max_blocks = max_blocks;
+  L.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, q, block_table, seq_lens, out,
+                                    workspace, L, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode launch");
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,187 @@
+// kv_quant_append: store new tokens' K/V into their physical blocks.
+//
+// Addressing follows the paged KV cache of the TFFInfer article (section
+// 3.6.4: logical token t -> slot t % block_size of block page_table[t /
+// block_size]); the quantiser is the asymmetric per-channel formula of the
+// heterogeneous engine article (section 2.6), applied per (physical block,
+// kv head, channel) as in its section 2.4.
+//
+// This translation unit is compiled with --fmad=false and uses explicitly
+// rounded intrinsics so every fp32 step is one IEEE operation in the stated
+// order: codes, scales and zero points are bit-exact across implementations.
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ int32_t sat_rint_i32(float x) {
+  // rintf then convert; cvt.rni.s32.f32 saturates and maps NaN to 0.
+  return __float2int_rn(x);
+}
+
+template <int KV>
+__device__ __forceinline__ int read_code(const uint8_t* page_codes, int D, int slot, int c) {
+  if (KV == PA_KV_UINT8) return page_codes[slot * D + c];
+  const uint8_t byte = page_codes[slot * (D / 2) + c / 2];
+  return (c & 1) ? (byte >> 4) : (byte & 15);
+}
+
+// One thread block per (sequence, touched-block slot x, tensor/head z); one
+// thread per channel. grid = (X, batch, 2 * Hkv), block = head_dim threads.
+template <int KV, int BS>
+__global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv_bfloat16* k_new,
+                                                        const __nv_bfloat16* v_new,
+                                                        const int32_t* cu_new,
+                                                        const int32_t* ctx_lens,
+                                                        const int32_t* block_table,
+                                                        int32_t max_blocks) {
+  // programmatic stream serialization: start early, touch memory only after
+  // the preceding kernel has completed
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int is_v = blockIdx.z & 1;
+  const int h = blockIdx.z >> 1;
+  const int c = threadIdx.x;
+  const int D = pool.head_dim;
+  const int Hkv = pool.num_kv_heads;
+
+  const int32_t c0 = cu_new[b], c1 = cu_new[b + 1];
+  const int n_new = c1 - c0;
+  if (n_new < 0) {
+    if (blockIdx.x == 0 && c == 0 && blockIdx.z == 0) set_error(pool.err, PA_DEVERR_APPEND);
+    return;
+  }
+  if (n_new == 0) return;
+  const int ctx = ctx_lens[b];
+  const long long total = (long long)ctx + n_new;
+  if (ctx < 0 || total > (long long)max_blocks * BS) {
+    if (blockIdx.x == 0 && c == 0 && blockIdx.z == 0) set_error(pool.err, PA_DEVERR_SEQ_LEN);
+    return;
+  }
+  const int first_blk = ctx / BS;
+  const int last_blk = (int)((total - 1) / BS);
+  const __nv_bfloat16* src = is_v ? v_new : k_new;
+  uint8_t* codes = is_v ? pool.v : pool.k;
+  float* scales = is_v ? pool.v_scale : pool.k_scale;
+  int32_t* zps = is_v ? pool.v_zp : pool.k_zp;
+
+  for (int blk = first_blk + blockIdx.x; blk <= last_blk; blk += gridDim.x) {
+    const int phys = block_table[(long long)b * max_blocks + blk];
+    if (phys < 0 || phys >= pool.num_blocks) {
+      if (c == 0 && !is_v && h == 0) set_error(pool.err, PA_DEVERR_BLOCK_TABLE);
+      continue;
+    }
+    const int first = blk * BS;
+    const int old_cnt = ctx > first ? min(ctx - first, BS) : 0;
+    const int valid = (int)min((long long)BS, total - first);
+    const long long page = (long long)phys * Hkv + h;
+    // row of the new-token array holding logical position first + s
+    const long long row0 = (long long)c0 + first - ctx;
+
+    if (KV == PA_KV_BF16) {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(codes) + page * BS * D;
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+      for (int s = old_cnt; s < valid; ++s)
+        dst[s * D + c] = s16[((row0 + s) * Hkv + h) * D + c];
+      continue;
+    }
+
+    constexpr int L = (KV == PA_KV_UINT4) ? 15 : 255;
+    uint8_t* pc = codes + page * BS * (KV == PA_KV_UINT4 ? D / 2 : D);
+    float vals[BS];
+    const float old_scale = scales[page * D + c];
+    const int32_t old_zp = zps[page * D + c];
+#pragma unroll
+    for (int s = 0; s < BS; ++s) {
+      float x = 0.0f;
+      if (s < old_cnt) {
+        const int32_t diff = read_code<KV>(pc, D, s, c) - old_zp;
+        x = __fmul_rn(__int2float_rn(diff), old_scale);
+      } else if (s < valid) {
+        x = __bfloat162float(src[((row0 + s) * Hkv + h) * D + c]);
+      }
+      vals[s] = x;
+    }
+    float mn = vals[0], mx = vals[0];
+#pragma unroll
+    for (int s = 1; s < BS; ++s) {
+      if (s < valid) {
+        if (vals[s] < mn) mn = vals[s];
+        if (vals[s] > mx) mx = vals[s];
+      }
+    }
+    const float r = __fsub_rn(mx, mn);
+    float scale = __fdiv_rn(r, (float)L);
+    if (!(scale > 0.0f)) {
+      scale = __fdiv_rn(fabsf(mn), (float)L);
+      if (!(scale > 0.0f)) scale = 1.0f;
+    }
+    const int32_t zp = sat_rint_i32(rintf(__fdiv_rn(-mn, scale)));
+    int code[BS];
+#pragma unroll
+    for (int s = 0; s < BS; ++s) {
+      long long t = (long long)sat_rint_i32(rintf(__fdiv_rn(vals[s], scale))) + (long long)zp;
+      t = t < 0 ? 0 : (t > L ? L : t);
+      code[s] = (int)t;
+    }
+    if (KV == PA_KV_UINT8) {
+#pragma unroll
+      for (int s = 0; s < BS; ++s)
+        if (s < valid) pc[s * D + c] = (uint8_t)code[s];
+    } else {
+      // pair channels 2i (low nibble) and 2i+1 (high nibble) of one byte
+#pragma unroll
+      for (int s = 0; s < BS; ++s) {
+        const int other = __shfl_xor_sync(0xffffffffu, code[s], 1);
+        if (s < valid && (c & 1) == 0) pc[s * (D / 2) + c / 2] = (uint8_t)(code[s] | (other << 4));
+      }
+    }
+    scales[page * D + c] = scale;
+    zps[page * D + c] = zp;
+  }
+}
+
+template <int KV, int BS>
+cudaError_t launch_append_t(const PoolDev& pool, const void* k_new, const void* v_new,
+                            const int32_t* cu_new, const int32_t* ctx_lens,
+                            const int32_t* block_table, int batch, int max_blocks,
+                            int blocks_per_seq, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks_per_seq, batch, 2 * pool.num_kv_heads);
+  cfg.blockDim = dim3(pool.head_dim);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_append_kernel<KV, BS>, pool,
+                            static_cast<const __nv_bfloat16*>(k_new),
+                            static_cast<const __nv_bfloat16*>(v_new), cu_new, ctx_lens, block_table,
+                            max_blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_append(int kv_dtype, const PoolDev& pool, const void* k_new, const void* v_new,
+                          const int32_t* cu_new, const int32_t* ctx_lens,
+                          const int32_t* block_table, int batch, int max_blocks,
+                          int blocks_per_seq, cudaStream_t stream) {
+#define PA_APPEND_CASE(KVT, BSV)                                                              \
+  if (kv_dtype == KVT && pool.block_size == BSV)                                              \
+    return launch_append_t<KVT, BSV>(pool, k_new, v_new, cu_new, ctx_lens, block_table, batch, \
+                                     max_blocks, blocks_per_seq, stream);
+  PA_APPEND_CASE(PA_KV_BF16, 16)
+  PA_APPEND_CASE(PA_KV_BF16, 32)
+  PA_APPEND_CASE(PA_KV_UINT8, 16)
+  PA_APPEND_CASE(PA_KV_UINT8, 32)
+  PA_APPEND_CASE(PA_KV_UINT4, 16)
+  PA_APPEND_CASE(PA_KV_UINT4, 32)
+#undef PA_APPEND_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -1,0 +1,43 @@
+// Internal launch interface between the C ABI (pa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct PoolDev;
+
+// Geometry of the decode launch: how the (sequence, kv head, block) work
+// list is cut into partitions and where partial results go.
+struct DecodeLaunch {
+  int num_ctas;         // partitions = thread blocks of the decode kernel
+  int group;            // Hq / Hkv
+  int num_q_heads;
+  int batch;
+  int max_blocks;
+  float scale_log2;     // softmax_scale * log2(e)
+  // workspace carve-up
+  int32_t* pre_pages;   // [batch + 1] prefix sums of per-sequence block counts
+  float* part_o;        // [num_ctas + batch*Hkv][group][D]
+  float* part_lse;      // [num_ctas + batch*Hkv][group]
+};
+
+cudaError_t launch_append(int kv_dtype, const PoolDev& pool, const void* k_new, const void* v_new,
+                          const int32_t* cu_new, const int32_t* ctx_lens,
+                          const int32_t* block_table, int batch, int max_blocks,
+                          int blocks_per_seq, cudaStream_t stream);
+
+// Bytes of workspace for a given partition count.
+size_t decode_workspace_bytes(int num_ctas, int batch, int num_kv_heads, int group, int head_dim);
+
+// Thread blocks of the decode kernel that fit on one SM for this shape.
+int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group);
+
+// Carve the workspace and launch decode + combine.
+cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const void* q,
+                          const int32_t* block_table, const int32_t* seq_lens, float* out,
+                          void* workspace, DecodeLaunch& L, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,129 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs. Quantised append must match bit-exactly (codes, scales,
+zero points); decode within max-abs 2e-3 and per-row relative 1e-2."""
+import numpy as np
+import pytest
+
+from paged_gqa_decode_02_gb300 import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_gqa_decode_02_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 3, 1000])
+def test_tiny_config(splits):
+    wl = W.tiny()
+    g, o = H.load_both(wl)
+    H.assert_pools_equal(g, o)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    got = H.gpu_decode(g, wl, num_splits=splits)
+    H.check_attention(got, ref, f"tiny splits={splits}")
+    assert g.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("seed", range(8))
+def test_random_small(seed, dt):
+    wl = W.random_small(seed, dt)
+    g, o = H.load_both(wl)
+    H.assert_pools_equal(g, o)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    for splits in (0, 1, 5, 10 ** 4):
+        got = H.gpu_decode(g, wl, num_splits=splits)
+        H.check_attention(got, ref, f"{wl.name} {dt} splits={splits}")
+    assert g.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+def test_multi_step_tail_requant(dt):
+    """Several decode steps, each appending one token per sequence into a
+    partly filled block (re-quantised), then attending."""
+    wl = W.make_case("steps", 31, 3, 8, 2, 128, 16, dt, [20, 33, 7], extra_blocks=3,
+                     channel_offset_sigma=0.5 if dt != "bf16" else None)
+    g, o = H.make_pools(wl)
+    first = wl.fill_calls(leave_last=True)[0]
+    H.gpu_append(g, first)
+    assert o.append_call(first) == 0
+    step = wl.step_call()
+    for _ in range(3):
+        H.gpu_append(g, step)
+        assert o.append_call(step) == 0
+        H.assert_pools_equal(g, o)
+        ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+        H.check_attention(H.gpu_decode(g, wl), ref, f"steps {dt}")
+
+
+def test_empty_and_single_token_sequences():
+    wl = W.make_case("edge", 41, 5, 12, 4, 64, 16, "bf16", [0, 1, 16, 0, 17], extra_blocks=2)
+    g, o = H.load_both(wl, leave_last=False)
+    ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    for splits in (0, 1, 7):
+        got = H.gpu_decode(g, wl, num_splits=splits)
+        H.check_attention(got, ref, f"edge splits={splits}")
+        assert np.all(got.reshape(5, 12, 64)[[0, 3]] == 0)
+
+
+def test_bad_table_entry_sets_error_word_and_gpu_stays_usable():
+    from paged_gqa_decode_02_gb300 import binding as B
+    wl = W.random_small(3, "uint8")
+    g, o = H.load_both(wl)
+    bad = wl.block_table.copy()
+    bad[0, 0] = wl.num_blocks + 5
+    torch = H.torch_mod()
+    out = torch.zeros((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
+    g.decode(H.dev(wl.q_bits), H.dev(bad), H.dev(wl.seq_lens), wl.softmax_scale, out=out)
+    st, flags = g.device_error()
+    assert st == 5 and flags & B.DEVERR_BLOCK_TABLE
+    bad_len = wl.seq_lens.copy()
+    bad_len[-1] = wl.max_blocks * wl.block_size + 1
+    g.decode(H.dev(wl.q_bits), H.dev(wl.block_table), H.dev(bad_len), wl.softmax_scale, out=out)
+    st, flags = g.device_error()
+    assert st == 5 and flags & B.DEVERR_SEQ_LEN
+    # a clean call afterwards is still correct
+    ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    H.check_attention(H.gpu_decode(g, wl), ref, "after error")
+    assert g.device_error() == (0, 0)
+
+
+def test_host_validation_errors():
+    from paged_gqa_decode_02_gb300 import binding as B
+    wl = W.tiny()
+    g, _ = H.make_pools(wl)
+    torch = H.torch_mod()
+    q = H.dev(wl.q_bits)
+    with pytest.raises(B.PagedAttnError) as e:
+        g.decode(q[:, :3], H.dev(wl.block_table), H.dev(wl.seq_lens), 0.125)  # 3 heads, Hkv = 2
+    assert e.value.status == 1
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.PagedAttnError) as e:
+        g.decode(q, H.dev(wl.block_table), H.dev(wl.seq_lens), 0.125, workspace=ws)
+    assert e.value.status == 3
+
+
+FULL = ["qwen25_7b_bf16", "qwen3_8b_int8", "long_uint4", "prefix_mix"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_config(name):
+    """Full-size workloads: the whole pool bit-exact after the bulk append and
+    the decode step's append; attention on sampled rows, in the automatic
+    launch configuration the benchmark times and with one forced split count."""
+    wl = W.CONFIGS[name]()
+    g, o = H.load_both(wl)
+    H.assert_pools_equal(g, o)
+    rows = H.sample_rows(wl)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    assert st == 0
+    for splits in (0, 97):
+        got = H.gpu_decode(g, wl, num_splits=splits)
+        H.check_attention(got[rows], ref, f"{name} splits={splits}")
+        assert np.isfinite(got).all()
+    assert g.device_error() == (0, 0)
