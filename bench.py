@@ -1,0 +1,372 @@
+"""Benchmark: one decode step of paged GQA attention per step -- append the
+step's new token of every sequence (kv_quant_append), then attend
+(paged_gqa_decode + split-KV combine) -- on the Qwen2.5-7B-shaped workload
+(batch 32, 28 Q / 4 KV heads, head_dim 128, block 16, seq_lens U[512, 4096],
+bf16 KV), synthetic seeded data.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--splits S]
+
+Prints one JSON line. value = decode tokens per second (batch / step time),
+whole job over all ranks. The L2 cache is flushed (a 256 MiB write) between
+timed steps, outside the per-step CUDA-event brackets. Under torchrun every
+rank runs its own replica of the workload (the path needs no exchange between
+GPUs): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attention: tokens/s and achieved HBM GB/s (% of GB300 peak)"
+WORKLOAD_TEXT = {
+    "qwen25_7b_bf16": "Qwen2.5-7B-shaped decode: batch 32, 28 Q / 4 KV heads, head_dim 128, block 16, "
+                      "seq_lens U[512,4096], bf16 KV",
+    "qwen3_8b_int8": "Qwen3-8B-shaped uint8 KV: batch 64, 32 Q / 8 KV heads, head_dim 128, block 16, "
+                     "seq_lens U[1,8192]",
+    "long_uint4": "long-context uint4 KV: batch 4, 32 Q / 8 KV heads, head_dim 128, block 32, 32768 tokens each",
+    "prefix_mix": "continuous-batching mix with prefix cache: batch 256, 28 Q / 4 KV heads, head_dim 128, "
+                  "block 16, lognormal(median 1000) lengths, 8x32 sequences share 512-token prefixes, bf16 KV",
+    "tiny": "tiny: batch 2, 4 Q / 2 KV heads, head_dim 64, block 16, seq_lens {37,5}, bf16 KV",
+}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+        return dist, int(os.environ.get("RANK", "0")), ws
+    return None, 0, 1
+
+
+def _max_over_ranks(dist, x):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def run_ours(args):
+    import torch
+    from paged_gqa_decode_02_gb300 import build as pbuild
+    from paged_gqa_decode_02_gb300 import workloads as W
+    from paged_gqa_decode_02_gb300.binding import PagedKVPool
+    from paged_gqa_decode_02_gb300.metrics import decode_bytes
+
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0:
+        pbuild.build()
+    _barrier(dist)
+    wl = W.CONFIGS[args.workload]()
+    dev = torch.device("cuda", local)
+    pool = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, local)
+
+    def d(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    for c in wl.fill_calls(leave_last=True):
+        pool.append_kv(d(c.k_bits), d(c.v_bits), d(c.cu_new), d(c.ctx_lens), d(c.block_table),
+                       max_new_per_seq=c.max_new)
+    step = wl.step_call()
+    st_k, st_v, st_cu, st_ctx = d(step.k_bits), d(step.v_bits), d(step.cu_new), d(step.ctx_lens)
+    table, seq_lens, q = d(wl.block_table), d(wl.seq_lens), d(wl.q_bits)
+    B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = pool.workspace(B, Hq, args.splits)
+    splits_used = pool.num_splits(args.splits)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        pool.append_kv(st_k, st_v, st_cu, st_ctx, table, max_new_per_seq=1)
+        e_mid = torch.cuda.Event(enable_timing=True)
+        e_mid.record(stream)
+        pool.decode(q, table, seq_lens, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
+        return e_mid
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        one_step()
+    torch.cuda.synchronize()
+    st, flags = pool.device_error()
+    assert st == 0 and flags == 0, f"device error word {flags:#x} during warm-up"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # soak so that the clock record covers a loaded GPU before and during timing
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        flush.fill_(1)
+        one_step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = []
+    _barrier(dist)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(1)
+        e0[i].record(stream)
+        e1.append(one_step())
+        e2[i].record(stream)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    clk = clocks.stop()
+    step_ms = [e0[i].elapsed_time(e2[i]) for i in range(K)]
+    dec_ms = [e1[i].elapsed_time(e2[i]) for i in range(K)]
+    st, flags = pool.device_error()
+    assert st == 0 and flags == 0, f"device error word {flags:#x} during timing"
+    t_step = statistics.mean(step_ms) / 1e3
+    t_dec = statistics.mean(dec_ms) / 1e3
+    t_step_max = _max_over_ranks(dist, t_step)
+    t_dec_max = _max_over_ranks(dist, t_dec)
+
+    # ---- e2e through the public API with host buffers (pinned), copies inside the region
+    h_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else
+                                np.ascontiguousarray(v)).pin_memory()
+            for k, v in (("k", step.k_bits), ("v", step.v_bits), ("cu", step.cu_new), ("ctx", step.ctx_lens),
+                         ("table", wl.block_table), ("lens", wl.seq_lens), ("q", wl.q_bits))}
+    h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    bi = sum(v.numel() * v.element_size() for v in h_in.values())
+    bo = h_out.numel() * h_out.element_size()
+    Ke = max(10, min(K, 200))
+    e2e_ms = []
+    for i in range(Ke + 3):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in d_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        pool.append_kv(d_in["k"], d_in["v"], d_in["cu"], d_in["ctx"], d_in["table"], max_new_per_seq=1)
+        pool.decode(d_in["q"], d_in["table"], d_in["lens"], wl.softmax_scale, out=out, workspace=ws,
+                    num_splits=args.splits)
+        h_out.copy_(out, non_blocking=True)
+        z.record(stream)
+        z.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(z))
+    t_e2e = _max_over_ranks(dist, statistics.mean(e2e_ms) / 1e3)
+
+    nb = decode_bytes(wl)
+    peak, peak_kind = _peaks()
+    achieved = nb["algorithmic"] / t_dec_max / 1e9
+    res = {
+        "metric": METRIC,
+        "value": world * B / t_step_max,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": t_step_max * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == "bf16" else f"{wl.kv_dtype} codes, fp32 math",
+        "data": "synthetic (seeded N(0,1) bf16 q/K/V, block tables from a seeded permutation)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": B,
+                   "num_q_heads": Hq, "num_kv_heads": wl.num_kv_heads, "head_dim": D,
+                   "block_size": wl.block_size, "kv_dtype": wl.kv_dtype,
+                   "tokens_cached": nb["tokens_scanned"], "num_splits": splits_used,
+                   "step": "append 1 token/seq (kv_quant_append) + paged_gqa_decode + combine",
+                   "l2": "flushed before every timed step (256 MiB write, outside the event brackets)",
+                   "parallelism": f"replicas x{world} (no exchange)"},
+        "hbm_gbs": achieved,
+        "decode_us": t_dec_max * 1e6,
+        "kv_tokens_per_s": world * nb["tokens_scanned"] / t_dec_max,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": nb["algorithmic"],
+                     "timed": "pa_decode call (decode kernel + split-KV combine), CUDA events on the launch stream"},
+        "e2e": {"value": world * B / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seqs)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    pool.close()
+
+
+def _oracle_setup(wl, n_seq):
+    """Oracle pool holding the first n_seq sequences' caches (setup, untimed)."""
+    from oracle import oracle
+    o = oracle.OraclePool(wl.kv_dtype, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    for c in wl.fill_calls(leave_last=True):
+        o.append_call(c)
+    step = wl.step_call()
+    keep = np.arange(n_seq)
+    rows = np.concatenate([np.arange(b * wl.num_q_heads, (b + 1) * wl.num_q_heads) for b in keep]).astype(np.int64)
+    cu = np.concatenate([[0], np.cumsum(np.diff(step.cu_new)[keep])]).astype(np.int32)
+    sel = np.concatenate([np.arange(step.cu_new[b], step.cu_new[b + 1]) for b in keep]).astype(np.int64)
+    sub = (step.k_bits[sel], step.v_bits[sel], cu, step.ctx_lens[keep], step.block_table[keep])
+    return o, sub, rows
+
+
+def _oracle_step(wl, o, sub, rows):
+    st = o.append(*sub)
+    out, st2 = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    assert st == 0 and st2 == 0
+    return out
+
+
+def cpu_baseline(wl, n_seq):
+    from oracle import oracle
+    n_seq = min(n_seq, wl.batch)
+    o, sub, rows = _oracle_setup(wl, n_seq)
+    _oracle_step(wl, o, sub, rows)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(wl, o, sub, rows)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 20:
+            break
+    t = (time.perf_counter() - t0) / reps
+    return {"value": n_seq / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n_seq} of {wl.batch} sequences (all {wl.num_q_heads} heads each), "
+                      f"append + decode step, mean of {reps} steps"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    from paged_gqa_decode_02_gb300 import workloads as W
+    from oracle import oracle
+
+    dist, rank, world = _dist()
+    if rank != 0:
+        return
+    wl = W.CONFIGS[args.workload]()
+    n_seq = min(args.cpu_seqs, wl.batch)
+    o, sub, rows = _oracle_setup(wl, n_seq)
+    for _ in range(max(3, args.warmup)):
+        _oracle_step(wl, o, sub, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_step(wl, o, sub, rows)
+        times.append(time.perf_counter() - t0)
+        if sum(times) > 120:
+            break
+    t = statistics.mean(times)
+    v = n_seq / t
+    res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+           "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quantisation steps)",
+           "data": "synthetic (same seeded workload)",
+           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                            "sample": f"{n_seq} of {wl.batch} sequences per step (all heads), append + decode"},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen25_7b_bf16", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--cpu-seqs", type=int, default=1 << 30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -157,6 +157,15 @@ PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int3
 /* Resolve num_splits = 0 to the partition count pa_decode would use. */
 PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
 
+/* Decode kernel selection for a pool. AUTO uses the tensor-core kernel where
+ * it is built (bf16 pools: scores and P.V as mma.m16n8k16 over the GQA group,
+ * pages staged by swizzled 2-D TMA) and the CUDA-core kernel otherwise;
+ * CUDA_CORE forces the fp32 FMA kernel (kept for comparison). Both compute
+ * the same operation. PA_ERR_UNSUPPORTED if TENSOR_CORE is asked for a pool
+ * it does not serve. */
+typedef enum { PA_DECODE_AUTO = 0, PA_DECODE_CUDA_CORE = 1, PA_DECODE_TENSOR_CORE = 2 } pa_decode_path;
+PA_API pa_status pa_pool_set_decode_path(pa_pool* pool, int32_t path);
+
 /* Device addresses of the pool's arrays, for inspection and tests. */
 PA_API pa_status pa_pool_view(const pa_pool* pool, pa_pool_buffers* out);
 

@@ -73,6 +73,8 @@ def lib():
         L.pa_decode.argtypes = [P, P, P, P, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
         L.pa_decode_workspace_bytes.argtypes = [P, I32, I32, I32]
         L.pa_decode_workspace_bytes.restype = SZ
+        L.pa_pool_set_decode_path.argtypes = [P, I32]
+        L.pa_pool_set_decode_path.restype = I32
         L.pa_decode_num_splits.argtypes = [P, I32]
         L.pa_decode_num_splits.restype = I32
         L.pa_pool_view.argtypes = [P, ctypes.POINTER(pa_pool_buffers)]
@@ -132,6 +134,14 @@ def pa_decode(handle, q, block_table, seq_lens, batch, num_q_heads, max_blocks, 
 
 def pa_decode_workspace_bytes(handle, batch, num_q_heads, num_splits=0):
     return int(lib().pa_decode_workspace_bytes(handle, int(batch), int(num_q_heads), int(num_splits)))
+
+
+PA_DECODE_AUTO, PA_DECODE_CUDA_CORE, PA_DECODE_TENSOR_CORE = 0, 1, 2
+DECODE_PATHS = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
+
+
+def pa_pool_set_decode_path(handle, path):
+    _check(lib().pa_pool_set_decode_path(handle, DECODE_PATHS[path] if isinstance(path, str) else int(path)))
 
 
 def pa_decode_num_splits(handle, num_splits=0):
@@ -199,6 +209,10 @@ class PagedKVPool:
         B = int(ctx_lens.shape[0])
         pa_append_kv(self.handle, k_new, v_new, cu_new, ctx_lens, block_table, B,
                      int(block_table.shape[1]) if B else 0, max_new_per_seq, stream)
+
+    def set_decode_path(self, path):
+        """'auto', 'cuda_core' or 'tensor_core' (see pa_pool_set_decode_path)."""
+        pa_pool_set_decode_path(self.handle, path)
 
     def workspace_bytes(self, batch, num_q_heads, num_splits=0):
         return pa_decode_workspace_bytes(self.handle, batch, num_q_heads, num_splits)

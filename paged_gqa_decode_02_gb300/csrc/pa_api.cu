@@ -10,7 +10,9 @@
 #include "pagedattn.h"
 
 struct pa_pool {
+  pa::PoolMaps maps;  // first: 64-byte aligned member
   pa_pool_desc desc;
+  int32_t decode_path;
   void* slab;
   size_t slab_bytes;
   pa::PoolDev dev;
@@ -56,9 +58,13 @@ struct DeviceGuard {
   }
 };
 
+bool uses_tensor_cores(const pa_pool* p) {
+  return p->desc.kv_dtype == PA_KV_BF16 && p->maps.valid && p->decode_path != PA_DECODE_CUDA_CORE;
+}
+
 int auto_splits(const pa_pool* p, int group) {
   return p->sm_count * pa::decode_ctas_per_sm(p->desc.kv_dtype, p->desc.block_size,
-                                              p->desc.head_dim, group);
+                                              p->desc.head_dim, group, uses_tensor_cores(p));
 }
 
 }  // namespace
@@ -151,6 +157,9 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
     delete p;
     return cuda_fail(e, "pool initialisation");
   }
+  p->decode_path = PA_DECODE_AUTO;
+  p->maps.valid = 0;
+  if (d->kv_dtype == PA_KV_BF16) pa::make_pool_maps(p->dev, p->maps);
   *out = p;
   return PA_OK;
 }
@@ -221,6 +230,17 @@ pa_status pa_append_kv(pa_pool* p, const void* k_new, const void* v_new, const i
   return PA_OK;
 }
 
+pa_status pa_pool_set_decode_path(pa_pool* p, int32_t path) {
+  g_last_error[0] = 0;
+  if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  if (path < PA_DECODE_AUTO || path > PA_DECODE_TENSOR_CORE)
+    return fail(PA_ERR_INVALID_ARG, "unknown decode path%s");
+  if (path == PA_DECODE_TENSOR_CORE && !(p->desc.kv_dtype == PA_KV_BF16 && p->maps.valid))
+    return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path needs a bf16 pool%s");
+  p->decode_path = path;
+  return PA_OK;
+}
+
 int32_t pa_decode_num_splits(const pa_pool* p, int32_t num_splits) {
   if (!p || num_splits < 0) return 0;
   return num_splits > 0 ? num_splits : auto_splits(p, 8);
@@ -267,7 +287,8 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   L.batch = batch;
   L.max_blocks = max_blocks;
   L.scale_log2 = softmax_scale * 1.4426950408889634f;
-  cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, q, block_table, seq_lens, out,
+  L.tensor_cores = uses_tensor_cores(p);
+  cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
                                     workspace, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode launch");
   return PA_OK;

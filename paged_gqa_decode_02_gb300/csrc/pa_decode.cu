@@ -31,6 +31,8 @@
 // (so no thread is stranded) and drains its outstanding copies before exit.
 #include <float.h>
 
+#include <type_traits>
+
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
@@ -38,9 +40,15 @@ namespace pa {
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxSegs = 64;
+// Consumer warps per thread block: the tensor-core consumer is short but
+// latency-bound, so it runs twice as many warps to keep each scheduler busy.
+template <bool TC>
+constexpr int consumer_warps() {
+  return TC ? 8 : 4;
+}
+constexpr int kMaxSegs = 64;         // segments per window
+constexpr int kMaxWinPages = 1024;   // pages per window (block-table entries staged in smem)
+constexpr int kContPrev = 1, kContNext = 2;
 
 // One contiguous run of pages of one unit inside a thread block's slice.
 struct Seg {
@@ -50,7 +58,8 @@ struct Seg {
   int32_t k0;        // index of the run's first page within the slice
   int32_t len;       // sequence length (tokens)
   int32_t slot;      // partial slot (cta + unit), or -1 when written directly
-  int32_t pad;
+  int32_t flags;     // kContPrev: continues the previous window's last run;
+                     // kContNext: continues in the next window (no write yet)
 };
 
 template <int KV, int D, int BS>
@@ -68,27 +77,29 @@ struct PageGeom {
   static constexpr int kOffVz = kOffVs + kMetaBytes;
 };
 
-template <int KV, int D, int BS, int G, int NS>
+template <int KV, int D, int BS, int G, int NS, int W>
 struct Smem {
   using PG = PageGeom<KV, D, BS>;
-  static constexpr int kStages = kConsumerWarps * NS;
+  static constexpr int kStages = W * NS;
   static constexpr int kQBytes = G * D * 2;
   static constexpr size_t kOffBars = 0;  // full[kStages], empty[kStages], qfull[2], qempty[2]
   static constexpr size_t kBarBytes = (2 * kStages + 4) * 8;
   static constexpr size_t kOffFlags = kBarBytes;  // int32 per stage
   static constexpr size_t kOffSegs = (kOffFlags + kStages * 4 + 15) / 16 * 16;
   static constexpr size_t kOffPlan = kOffSegs + kMaxSegs * sizeof(Seg);  // 32 int64
-  static constexpr size_t kOffQ = (kOffPlan + 32 * 8 + 127) / 128 * 128;
+  static constexpr size_t kOffPhys = kOffPlan + 32 * 8;                   // int32 per window page
+  static constexpr size_t kOffQ = (kOffPhys + kMaxWinPages * 4 + 127) / 128 * 128;
   static constexpr size_t kOffStash = kOffQ + 2 * kQBytes;
-  static constexpr size_t kStashAccBytes = (size_t)kConsumerWarps * G * D * 4;
+  static constexpr size_t kStashAccBytes = (size_t)W * G * D * 4;
   static constexpr size_t kOffStashML = kOffStash + kStashAccBytes;
-  static constexpr size_t kOffPbuf = kOffStashML + kConsumerWarps * G * 2 * 4;
-  static constexpr size_t kPbufBytes = (size_t)kConsumerWarps * BS * G * 4;
-  static constexpr size_t kOffStages = (kOffPbuf + kPbufBytes + 127) / 128 * 128;
-  static constexpr size_t kBytes = kOffStages + (size_t)kStages * PG::kStageBytes;
+  static constexpr size_t kOffPbuf = kOffStashML + W * G * 2 * 4;
+  static constexpr size_t kPbufBytes = (size_t)W * BS * G * 4;
+  static constexpr size_t kOffStages = (kOffPbuf + kPbufBytes + 1023) / 1024 * 1024;
+  static constexpr size_t kBytes = kOffStages + (size_t)kStages * PG::kStageBytes + 1024;
 };
 
 struct DecodeParams {
+  PoolMaps maps;
   PoolDev pool;
   const uint16_t* q;
   const int32_t* block_table;
@@ -119,7 +130,7 @@ __device__ __forceinline__ long long owner_of(long long x, long long T, long lon
   return ((x + 1) * G - 1) / T;
 }
 
-// Block-wide inclusive scan of one int per thread (all kThreads threads call).
+// Block-wide inclusive scan of one int per thread (all threads call).
 __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -132,7 +143,7 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total)
   __syncthreads();
   int before = 0, tot = 0;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
     const int t = warp_tot[w];
     if (w < warp) before += t;
     tot += t;
@@ -316,14 +327,201 @@ struct FmaConsumer {
   }
 };
 
+
+// ------------------------------------------------------------------ consumer math (tensor cores)
+//
+// bf16 pools, pages staged by 2-D TMA with 128-byte swizzle: a page is
+// [D/64 halves][BS rows][128 B], and 16-byte chunk c of row r sits at chunk
+// c ^ (r % 8) of its 128-byte row, so ldmatrix reads are conflict-free.
+//
+// Scores of 16 tokens x the 8-wide head group come from mma.m16n8k16
+// (A = K rows, B = Q^T held in registers for the whole unit, fp32
+// accumulate). P.V uses A = V^T (ldmatrix.trans) and B = P^T, obtained from
+// the score fragments with movmatrix.trans. P is split into a bf16 high part
+// and a bf16 remainder (two mma per tile) so the weights keep ~16 bits.
+// Lane t holds heads 2(t%4), 2(t%4)+1 throughout: the online-softmax state
+// and the O^T accumulator columns line up without any exchange.
+template <int D, int BS, int G>
+struct MmaConsumerBf16 {
+  static constexpr int KS = D / 16;   // k-steps of the score mma
+  static constexpr int MT = D / 16;   // channel tiles of the P.V mma
+  static constexpr int TT = BS / 16;  // 16-token tiles per page
+  static constexpr int HALF_BYTES = BS * 128;
+  static_assert(G <= 8, "head group");
+
+  uint32_t qf[KS][2];
+  float o[MT][4];
+  float m0, m1, l0, l1;
+  float scale_log2;
+
+  __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
+    const int lane = threadIdx.x & 31;
+    const int h = lane >> 2, c2 = (lane & 3) * 2;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b0 = 0, b1 = 0;
+      if (h < g) {
+        b0 = *reinterpret_cast<const uint32_t*>(q_smem + h * D + ks * 16 + c2);
+        b1 = *reinterpret_cast<const uint32_t*>(q_smem + h * D + ks * 16 + c2 + 8);
+      }
+      qf[ks][0] = b0;
+      qf[ks][1] = b1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.0f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.0f;
+    scale_log2 = sl2;
+  }
+
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t kb = smem_u32(stage);
+    const uint32_t vb = kb + 2 * (D / 64) * HALF_BYTES / 2;  // V follows K
+    // ---- scores S[token][head] for every 16-token tile
+    float s[TT][4];
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[tt][i] = 0.0f;
+      const int row = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int chunk = (ks & 3) * 2 + (lane >> 4);  // 16-byte chunk within the 128-byte half-row
+        const uint32_t addr = kb + (ks >> 2) * HALF_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4);
+        uint32_t a[4];
+        ldmatrix_x4(a, addr);
+        mma_bf16_16816(s[tt], a, qf[ks][0], qf[ks][1]);
+      }
+    }
+    // ---- online softmax for heads 2(t%4) and 2(t%4)+1
+    const int tok = lane >> 2;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const bool v0 = tt * 16 + tok < valid, v1 = tt * 16 + tok + 8 < valid;
+      s[tt][0] = v0 ? s[tt][0] * scale_log2 : -INFINITY;
+      s[tt][1] = v0 ? s[tt][1] * scale_log2 : -INFINITY;
+      s[tt][2] = v1 ? s[tt][2] * scale_log2 : -INFINITY;
+      s[tt][3] = v1 ? s[tt][3] * scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    uint32_t ph[TT][2], pl[TT][2];
+    float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
+      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      ps0 += p0 + p2;
+      ps1 += p1 + p3;
+      const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+      const uint32_t l01 = pack_bf16(p0 - bf16_lo_f(h01), p1 - bf16_hi_f(h01));
+      const uint32_t l23 = pack_bf16(p2 - bf16_lo_f(h23), p3 - bf16_hi_f(h23));
+      ph[tt][0] = movmatrix_trans(h01);
+      ph[tt][1] = movmatrix_trans(h23);
+      pl[tt][0] = movmatrix_trans(l01);
+      pl[tt][1] = movmatrix_trans(l23);
+    }
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      o[mt][0] *= a0;
+      o[mt][1] *= a1;
+      o[mt][2] *= a0;
+      o[mt][3] *= a1;
+    }
+    // ---- rows past the sequence end may hold anything: zero them so 0 * x
+    // cannot turn into NaN inside the P.V mma
+    if (valid < BS) {
+      uint8_t* vrow = stage + (D / 64) * HALF_BYTES;
+      const int n16 = (BS - valid) * (D / 64) * 8;
+      for (int i = lane; i < n16; i += 32) {
+        const int half = i / ((BS - valid) * 8);
+        const int rem = i % ((BS - valid) * 8);
+        const int r = valid + rem / 8, c = rem % 8;
+        *reinterpret_cast<uint4*>(vrow + half * HALF_BYTES + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // ---- O^T[channel][head] += V^T[channel][token] P^T[token][head]
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const int j = lane >> 3;
+      const int row = tt * 16 + (lane & 7) + (j >> 1) * 8;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int chunk = mt * 2 + (j & 1);  // 16-byte chunk across the 256-byte row
+        const int half = chunk >> 3, c = chunk & 7;
+        const uint32_t addr = vb + half * HALF_BYTES + row * 128 + ((c ^ (row & 7)) << 4);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, addr);
+        mma_bf16_16816(o[mt], a, ph[tt][0], ph[tt][1]);
+        mma_bf16_16816(o[mt], a, pl[tt][0], pl[tt][1]);
+      }
+    }
+    if (valid < BS) fence_proxy_async_smem();  // generic writes above, TMA writes next
+  }
+
+  __device__ __forceinline__ void deposit(float* st_acc, float* st_ml) {
+    const int lane = threadIdx.x & 31;
+    float s0 = l0, s1 = l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    const int h0 = (lane & 3) * 2, ch = lane >> 2;
+    if (lane < 4) {
+      if (h0 < G) {
+        st_ml[h0 * 2] = m0;
+        st_ml[h0 * 2 + 1] = s0;
+      }
+      if (h0 + 1 < G) {
+        st_ml[(h0 + 1) * 2] = m1;
+        st_ml[(h0 + 1) * 2 + 1] = s1;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      if (h0 < G) {
+        st_acc[h0 * D + mt * 16 + ch] = o[mt][0];
+        st_acc[h0 * D + mt * 16 + ch + 8] = o[mt][2];
+      }
+      if (h0 + 1 < G) {
+        st_acc[(h0 + 1) * D + mt * 16 + ch] = o[mt][1];
+        st_acc[(h0 + 1) * D + mt * 16 + ch + 8] = o[mt][3];
+      }
+    }
+  }
+};
+
 // ------------------------------------------------------------------ the decode kernel
-template <int KV, int D, int BS, int G, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_gqa_decode_kernel(const DecodeParams p) {
-  using SM = Smem<KV, D, BS, G, NS>;
+template <int KV, int D, int BS, int G, int NS, bool TC>
+__global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
+    paged_gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int kConsumerWarps = consumer_warps<TC>();
+  constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  using SM = Smem<KV, D, BS, G, NS, kConsumerWarps>;
   using PG = PageGeom<KV, D, BS>;
+  using Cons = typename std::conditional<TC, MmaConsumerBf16<D, BS, G>, FmaConsumer<KV, D, BS, G>>::type;
+  static_assert(!TC || KV == PA_KV_BF16, "tensor-core consumer reads bf16 pages");
   constexpr int NST = SM::kStages;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled TMA destinations
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kOffBars);
   uint64_t* empty = full + NST;
   uint64_t* qfull = empty + NST;
@@ -331,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* stage_flag = reinterpret_cast<int32_t*>(smem + SM::kOffFlags);
   Seg* segs = reinterpret_cast<Seg*>(smem + SM::kOffSegs);
   long long* plan = reinterpret_cast<long long*>(smem + SM::kOffPlan);
+  int32_t* phys_s = reinterpret_cast<int32_t*>(smem + SM::kOffPhys);
   uint8_t* qslots = smem + SM::kOffQ;
   float* stash_acc = reinterpret_cast<float*>(smem + SM::kOffStash);
   float* stash_ml = reinterpret_cast<float*>(smem + SM::kOffStashML);
@@ -341,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Hkv = p.pool.num_kv_heads;
   const int g = p.group;
   const long long Gc = gridDim.x, cta = blockIdx.x;
-  __shared__ int warp_tot[kThreads / 32];
-  __shared__ int abort_flag;
+  __shared__ int warp_tot[32];
+  __shared__ volatile int abort_flag;
   __shared__ int issued_n[NST];  // last fill issued per stage (drain on abort)
   __shared__ int q_issued[2];    // last q segment index issued per slot
 
@@ -415,12 +614,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long pos = s_i;
   int seg_counter = 0;      // segments started so far (q slot ring index)
   uint64_t pol = policy_evict_first();
+  Cons cons;  // consumer warps' online-softmax state; persists across windows
 
   while (pos < e_i) {
     // ---- build this window's segment list (warp 0)
     if (warp == 0) {
       int nseg = 0;
       long long b0 = cur_b, base0 = cur_base, wpos = pos;
+      const long long wlim = min(e_i, pos + (long long)kMaxWinPages);
       bool done = false;
       while (!done && b0 < p.batch) {
         const long long bb = b0 + lane;
@@ -434,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const long long my_base = base0 + (long long)(x - n) * Hkv;
         const long long my_end = my_base + (long long)n * Hkv;
-        const bool overl = n > 0 && my_end > wpos && my_base < e_i && bb < p.batch;
+        const bool overl = n > 0 && my_end > wpos && my_base < wlim && bb < p.batch;
         unsigned mask = __ballot_sync(0xffffffffu, overl);
         while (mask) {
           const int src = __ffs(mask) - 1;
@@ -444,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sn = __shfl_sync(0xffffffffu, n, src);
           const int slen = __shfl_sync(0xffffffffu, len, src);
           const int h_lo = (int)max(0LL, (wpos - sbase) / sn);
-          const int h_hi = (int)min((long long)Hkv - 1, (e_i - 1 - sbase) / sn);
+          const int h_hi = (int)min((long long)Hkv - 1, (wlim - 1 - sbase) / sn);
           for (int h = h_lo; h <= h_hi && !done; ++h) {
             const long long us = sbase + (long long)h * sn, ue = us + sn;
-            const long long lo = max(us, wpos), hi = min(ue, e_i);
+            const long long lo = max(us, wpos), hi = min(ue, wlim);
             if (lo >= hi) continue;
             if (lane == 0) {
               Seg sg;
@@ -459,15 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               sg.len = slen;
               const long long first = owner_of(us, T, Gc), last = owner_of(ue - 1, T, Gc);
               sg.slot = first == last ? -1 : (int)(cta + sb * Hkv + h);
-              sg.pad = 0;
+              // a unit's pages are contiguous within a slice: a run that starts
+              // after both the unit's and the slice's first page continues the
+              // previous window; one that stops before both ends goes on
+              sg.flags = (lo > us && lo > s_i ? kContPrev : 0) | (hi < ue && hi < e_i ? kContNext : 0);
               segs[nseg] = sg;
             }
             ++nseg;
             wpos = hi;
-            if (hi >= e_i) done = true;
-            if (nseg == kMaxSegs && !done) {
+            if (hi >= wlim || nseg == kMaxSegs) {
               done = true;
-              // resume at the sequence holding wpos
+              // the next window resumes at the sequence holding wpos
               if (wpos >= sbase + (long long)sn * Hkv) {
                 cur_b = sb + 1;
                 cur_base = sbase + (long long)sn * Hkv;
@@ -500,83 +703,102 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
       // ---------------------------------------------------------- producer
-      int si = 0;  // segment of the current page
-      int qseg = 0;
-      for (int kb = kw0; kb < kw1; kb += 32) {
-        const int my_k = kb + lane;
-        int my_phys = -1;
-        if (my_k < kw1) {
-          int s = 0;
-          while (s + 1 < nseg && my_k >= segs[s + 1].k0) ++s;
-          const Seg& sg = segs[s];
-          my_phys = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (my_k - sg.k0)];
+      // (1) the window's block-table entries -> shared memory, all lanes
+      {
+        int sx = 0;
+        for (int i = lane; i < kw1 - kw0; i += 32) {
+          const int k = kw0 + i;
+          while (sx + 1 < nseg && k >= segs[sx + 1].k0) ++sx;
+          const Seg& sg = segs[sx];
+          phys_s[i] = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
         }
-        const int cnt = min(32, kw1 - kb);
-        for (int j = 0; j < cnt; ++j) {
-          const int k = kb + j;
-          const int phys = __shfl_sync(0xffffffffu, my_phys, j);
-          while (si + 1 < nseg && k >= segs[si + 1].k0) ++si;
+        __syncwarp();
+      }
+      // (2) issue in sub-batches, lane j taking page k + j. A sub-batch holds
+      // at most one page per stage (<= NST pages): the previous fill of each
+      // lane's stage was issued by an earlier sub-batch, after the release of
+      // the fill before it, so each parity wait below sees its barrier at most
+      // one phase behind. (Two lanes on one stage could see a barrier two
+      // phases behind, take its parity for "released" and overwrite a stage
+      // still in use.) A sub-batch never crosses the start of a segment: the
+      // segment's q goes out first (lane 0).
+      int qseg = 0;
+      for (int k = kw0; k < kw1;) {
+        if (qseg < nseg && segs[qseg].k0 == k) {
           if (lane == 0) {
-            const Seg& sg = segs[si];
-            const bool aborted = abort_flag != 0;
-            // q of a unit goes out with its first page in this slice
-            while (qseg <= si) {
-              const int gs = seg_counter + qseg;
-              const int slot = gs & 1;
-              bool ok = true;
-              if (gs >= 2 && !aborted) ok = mbar_wait_bounded(&qempty[slot], ((gs >> 1) - 1) & 1);
-              if (!ok) {
-                set_error(p.pool.err, PA_DEVERR_TIMEOUT);
-                abort_flag = 1;
-              }
-              const Seg& qs = segs[qseg];
-              const uint16_t* qsrc = p.q + ((long long)qs.b * p.num_q_heads + (long long)qs.h * g) * D;
-              if (abort_flag) {
-                mbar_arrive(&qfull[slot]);
-              } else {
-                q_issued[slot] = gs;
-                mbar_arrive_expect_tx(&qfull[slot], g * D * 2);
-                bulk_g2s(qslots + slot * SM::kQBytes, qsrc, g * D * 2, &qfull[slot], pol);
-              }
-              ++qseg;
-            }
-            const int stage = k % NST;
-            const int n = k / NST;
+            const int gs = seg_counter + qseg;
+            const int slot = gs & 1;
             bool ok = true;
-            if (n >= 1 && !abort_flag) ok = mbar_wait_bounded(&empty[stage], (n - 1) & 1);
+            if (gs >= 2 && !abort_flag) ok = mbar_wait_bounded(&qempty[slot], ((gs >> 1) - 1) & 1);
             if (!ok) {
               set_error(p.pool.err, PA_DEVERR_TIMEOUT);
               abort_flag = 1;
             }
-            if (phys < 0 || phys >= p.pool.num_blocks || abort_flag) {
-              if (!abort_flag) set_error(p.pool.err, PA_DEVERR_BLOCK_TABLE);
-              stage_flag[stage] = 1;
-              mbar_arrive(&full[stage]);
+            const Seg& qs = segs[qseg];
+            const uint16_t* qsrc = p.q + ((long long)qs.b * p.num_q_heads + (long long)qs.h * g) * D;
+            if (abort_flag) {
+              mbar_arrive(&qfull[slot]);
             } else {
-              stage_flag[stage] = 0;
-              uint8_t* dst = stages + (size_t)stage * PG::kStageBytes;
-              const long long page = (long long)phys * Hkv + sg.h;
-              issued_n[stage] = n;
-              mbar_arrive_expect_tx(&full[stage], PG::kStageBytes);
-              bulk_g2s(dst + PG::kOffK, p.pool.k + page * PG::kPageBytes, PG::kPageBytes, &full[stage], pol);
-              bulk_g2s(dst + PG::kOffV, p.pool.v + page * PG::kPageBytes, PG::kPageBytes, &full[stage], pol);
-              if (KV != PA_KV_BF16) {
-                bulk_g2s(dst + PG::kOffKs, p.pool.k_scale + page * D, PG::kMetaBytes, &full[stage], pol);
-                bulk_g2s(dst + PG::kOffKz, p.pool.k_zp + page * D, PG::kMetaBytes, &full[stage], pol);
-                bulk_g2s(dst + PG::kOffVs, p.pool.v_scale + page * D, PG::kMetaBytes, &full[stage], pol);
-                bulk_g2s(dst + PG::kOffVz, p.pool.v_zp + page * D, PG::kMetaBytes, &full[stage], pol);
-              }
+              q_issued[slot] = gs;
+              mbar_arrive_expect_tx(&qfull[slot], g * D * 2);
+              bulk_g2s(qslots + slot * SM::kQBytes, qsrc, g * D * 2, &qfull[slot], pol);
             }
           }
+          ++qseg;
           __syncwarp();
         }
+        int kend = min(kw1, k + (NST < 32 ? NST : 32));
+        if (qseg < nseg) kend = min(kend, segs[qseg].k0);
+        const int kk = k + lane;
+        if (kk < kend) {
+          const Seg& sg = segs[qseg - 1];  // the sub-batch lies inside this segment
+          const int phys = phys_s[kk - kw0];
+          const int stage = kk % NST;
+          const int n = kk / NST;
+          bool ok = true;
+          if (n >= 1 && !abort_flag) ok = mbar_wait_bounded(&empty[stage], (n - 1) & 1);
+          if (!ok) {
+            set_error(p.pool.err, PA_DEVERR_TIMEOUT);
+            abort_flag = 1;
+          }
+          if (phys < 0 || phys >= p.pool.num_blocks || abort_flag) {
+            if (!abort_flag) set_error(p.pool.err, PA_DEVERR_BLOCK_TABLE);
+            stage_flag[stage] = 1;
+            mbar_arrive(&full[stage]);
+          } else {
+            stage_flag[stage] = 0;
+            uint8_t* dst = stages + (size_t)stage * PG::kStageBytes;
+            const long long page = (long long)phys * Hkv + sg.h;
+            issued_n[stage] = n;
+            mbar_arrive_expect_tx(&full[stage], PG::kStageBytes);
+            if (TC) {
+              // two 64-channel boxes per tensor (one for head_dim 64), swizzled
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf) {
+                tma_load_2d(dst + PG::kOffK + hf * BS * 128, &p.maps.k, hf * 64, (int)(page * BS),
+                            &full[stage], pol);
+                tma_load_2d(dst + PG::kOffV + hf * BS * 128, &p.maps.v, hf * 64, (int)(page * BS),
+                            &full[stage], pol);
+              }
+            } else {
+              bulk_g2s(dst + PG::kOffK, p.pool.k + page * PG::kPageBytes, PG::kPageBytes, &full[stage], pol);
+              bulk_g2s(dst + PG::kOffV, p.pool.v + page * PG::kPageBytes, PG::kPageBytes, &full[stage], pol);
+            }
+            if (KV != PA_KV_BF16) {
+              bulk_g2s(dst + PG::kOffKs, p.pool.k_scale + page * D, PG::kMetaBytes, &full[stage], pol);
+              bulk_g2s(dst + PG::kOffKz, p.pool.k_zp + page * D, PG::kMetaBytes, &full[stage], pol);
+              bulk_g2s(dst + PG::kOffVs, p.pool.v_scale + page * D, PG::kMetaBytes, &full[stage], pol);
+              bulk_g2s(dst + PG::kOffVz, p.pool.v_zp + page * D, PG::kMetaBytes, &full[stage], pol);
+            }
+          }
+        }
+        __syncwarp();
+        k = kend;
       }
-      // units without pages in this window never happen: every segment has >= 1 page
     } else {
       // ---------------------------------------------------------- consumers
       const int cw = warp - 1;
       float* pbuf = pbuf_all + cw * BS * G;
-      FmaConsumer<KV, D, BS, G> cons;
       for (int si = 0; si < nseg; ++si) {
         const Seg sg = segs[si];
         const int gs = seg_counter + si;
@@ -586,7 +808,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) set_error(p.pool.err, PA_DEVERR_TIMEOUT);
           abort_flag = 1;
         }
-        cons.begin_unit(reinterpret_cast<const uint16_t*>(qslots + slot * SM::kQBytes), g, p.scale_log2);
+        if (!(sg.flags & kContPrev))
+          cons.begin_unit(reinterpret_cast<const uint16_t*>(qslots + slot * SM::kQBytes), g, p.scale_log2);
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[slot]);
         // my pages: k = k0 + i with k % W == cw
@@ -607,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
         }
+        if (sg.flags & kContNext) continue;  // the run goes on in the next window
         cons.deposit(stash_acc + cw * G * D, stash_ml + cw * G * 2);
         named_bar_sync(1, kConsumerWarps * 32);
         // ---- merge the warps' states and write
@@ -655,22 +879,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 // were written by the decode kernel; empty sequences get zero rows; the rest
 // merge their partials: M = max_s lse_s, w_s = 2^(lse_s - M),
 // out = sum_s w_s o_s / sum_s w_s (the same algebra as the online-softmax
-// update, applied to whole partial states).
+// update, applied to whole partial states). The log-sum-exps of up to 32
+// slices are staged in shared memory with one round of loads.
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256)
     splitkv_combine_kernel(const int32_t* pre_pages, const float* part_o, const float* part_lse,
                            float* out, int batch, int num_kv_heads, int group, int num_q_heads,
                            int num_ctas) {
+  constexpr int kMaxSl = 32;
+  __shared__ float wgt[kMaxSl][8];
+  __shared__ float inv_tot[8];
   pdl_launch_dependents();
   pdl_wait();
-  const int u = blockIdx.x;
+  const int u = blockIdx.x, tid = threadIdx.x;
   const int b = u / num_kv_heads, j = u % num_kv_heads;
   const long long pre = pre_pages[b];
   const long long n = pre_pages[b + 1] - pre;
   const long long T = (long long)pre_pages[batch] * num_kv_heads;
   const long long row0 = (long long)b * num_q_heads + (long long)j * group;
   if (n == 0) {
-    for (int e = threadIdx.x; e < group * D; e += blockDim.x) out[row0 * D + e] = 0.0f;
+    for (int e = tid; e < group * D; e += blockDim.x) out[row0 * D + e] = 0.0f;
     return;
   }
   const long long us = pre * num_kv_heads + (long long)j * n;
@@ -683,28 +911,59 @@ __global__ void __launch_bounds__(128)
     const long long a = T * i / num_ctas, z = T * (i + 1) / num_ctas;
     return (a > us ? a : us) < (z < us + n ? z : us + n);
   };
-  for (int e = threadIdx.x; e < group * D; e += blockDim.x) {
-    const int h = e / D, c = e % D;
+  const long long nsl = last - first + 1;
+  if (nsl <= kMaxSl) {
+    if (tid < nsl * group) {
+      const int sl = tid / group, h = tid % group;
+      wgt[sl][h] = has_part(first + sl) ? part_lse[(first + sl + u) * group + h] : -INFINITY;
+    }
+    __syncthreads();
+    if (tid < group) {
+      float M = -INFINITY;
+      for (int sl = 0; sl < nsl; ++sl) M = fmaxf(M, wgt[sl][tid]);
+      float W = 0.0f;
+      for (int sl = 0; sl < nsl; ++sl) {
+        const float w = wgt[sl][tid] == -INFINITY ? 0.0f : exp2f(wgt[sl][tid] - M);
+        wgt[sl][tid] = w;
+        W += w;
+      }
+      inv_tot[tid] = W > 0.0f ? 1.0f / W : 0.0f;
+    }
+    __syncthreads();
+    for (int e = tid; e < group * D; e += blockDim.x) {
+      const int h = e / D;
+      float A = 0.0f;
+#pragma unroll 4
+      for (int sl = 0; sl < nsl; ++sl) {
+        const float w = wgt[sl][h];
+        if (w != 0.0f) A += w * part_o[(first + sl + u) * group * D + e];
+      }
+      out[row0 * D + e] = A * inv_tot[h];
+    }
+    return;
+  }
+  // many slices (forced large split counts): straightforward two-pass merge
+  for (int e = tid; e < group * D; e += blockDim.x) {
+    const int h = e / D;
     float M = -INFINITY;
     for (long long i = first; i <= last; ++i)
       if (has_part(i)) M = fmaxf(M, part_lse[(i + u) * group + h]);
     float W = 0.0f, A = 0.0f;
     for (long long i = first; i <= last; ++i) {
       if (!has_part(i)) continue;
-      const long long s = i + u;
-      const float l = part_lse[s * group + h];
+      const float l = part_lse[(i + u) * group + h];
       const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
       W += w;
-      A += w * part_o[(s * group + h) * D + c];
+      A += w * part_o[(i + u) * group * D + e];
     }
-    out[(row0 + h) * D + c] = W > 0.0f ? A / W : 0.0f;
+    out[row0 * D + e] = W > 0.0f ? A / W : 0.0f;
   }
 }
 
-template <int KV, int D, int BS, int G, int NS>
+template <int KV, int D, int BS, int G, int NS, bool TC>
 cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t stream) {
-  using SM = Smem<KV, D, BS, G, NS>;
-  auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS>;
+  using SM = Smem<KV, D, BS, G, NS, consumer_warps<TC>()>;
+  auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC>;
   static bool attr_set = false;  // per instantiation; set before first launch
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::kBytes);
@@ -716,7 +975,7 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.num_ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3((consumer_warps<TC>() + 1) * 32);
   cfg.dynamicSmemBytes = SM::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -726,7 +985,7 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   const int units = prm.batch * prm.pool.num_kv_heads;
   if (units == 0) return cudaSuccess;
   cfg.gridDim = dim3(units);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D>, (const int32_t*)prm.pre_pages,
                             (const float*)prm.part_o, (const float*)prm.part_lse, prm.out,
@@ -735,51 +994,90 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
 }
 
 // Stages per consumer warp: as many pages in flight as fit a ~160 KB ring
-// (2..4 per warp).
-template <int KV, int D, int BS>
+// (1..4 per warp; one only for 16 KB pages with eight consumer warps).
+template <int KV, int D, int BS, int W>
 constexpr int stages_per_warp() {
-  constexpr int n = (160 * 1024) / (kConsumerWarps * PageGeom<KV, D, BS>::kStageBytes);
-  return n < 2 ? 2 : (n > 4 ? 4 : n);
+  constexpr int n = (160 * 1024) / (W * PageGeom<KV, D, BS>::kStageBytes);
+  return n < 1 ? 1 : (n > 4 ? 4 : n);
+}
+
+template <int KV, int D, int BS, bool TC>
+cudaError_t dispatch_g(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
+  constexpr int NS = stages_per_warp<KV, D, BS, consumer_warps<TC>()>();
+  if (L.group <= 2) return launch_t<KV, D, BS, 2, NS, TC>(prm, L, s);
+  if (L.group <= 4) return launch_t<KV, D, BS, 4, NS, TC>(prm, L, s);
+  return launch_t<KV, D, BS, 8, NS, TC>(prm, L, s);
 }
 
 template <int KV, int D, int BS>
-cudaError_t dispatch_g(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
-  constexpr int NS = stages_per_warp<KV, D, BS>();
-  if (L.group <= 2) return launch_t<KV, D, BS, 2, NS>(prm, L, s);
-  if (L.group <= 4) return launch_t<KV, D, BS, 4, NS>(prm, L, s);
-  return launch_t<KV, D, BS, 8, NS>(prm, L, s);
+cudaError_t dispatch_path(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
+  if constexpr (KV == PA_KV_BF16) {
+    if (L.tensor_cores) return dispatch_g<KV, D, BS, true>(prm, L, s);
+  }
+  return dispatch_g<KV, D, BS, false>(prm, L, s);
 }
 
 template <int KV>
 cudaError_t dispatch_kv(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
   const int D = prm.pool.head_dim, BS = prm.pool.block_size;
-  if (D == 64 && BS == 16) return dispatch_g<KV, 64, 16>(prm, L, s);
-  if (D == 64 && BS == 32) return dispatch_g<KV, 64, 32>(prm, L, s);
-  if (D == 128 && BS == 16) return dispatch_g<KV, 128, 16>(prm, L, s);
-  if (D == 128 && BS == 32) return dispatch_g<KV, 128, 32>(prm, L, s);
+  if (D == 64 && BS == 16) return dispatch_path<KV, 64, 16>(prm, L, s);
+  if (D == 64 && BS == 32) return dispatch_path<KV, 64, 32>(prm, L, s);
+  if (D == 128 && BS == 16) return dispatch_path<KV, 128, 16>(prm, L, s);
+  if (D == 128 && BS == 32) return dispatch_path<KV, 128, 32>(prm, L, s);
   return cudaErrorInvalidValue;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-template <int KV, int D, int BS>
+template <int KV, int D, int BS, bool TC>
 size_t smem_bytes_g(int group) {
-  constexpr int NS = stages_per_warp<KV, D, BS>();
-  static_assert(Smem<KV, D, BS, 8, NS>::kBytes <= 227 * 1024, "shared memory budget");
-  if (group <= 2) return Smem<KV, D, BS, 2, NS>::kBytes;
-  if (group <= 4) return Smem<KV, D, BS, 4, NS>::kBytes;
-  return Smem<KV, D, BS, 8, NS>::kBytes;
+  constexpr int W = consumer_warps<TC>();
+  constexpr int NS = stages_per_warp<KV, D, BS, W>();
+  static_assert(Smem<KV, D, BS, 8, NS, W>::kBytes <= 227 * 1024, "shared memory budget");
+  if (group <= 2) return Smem<KV, D, BS, 2, NS, W>::kBytes;
+  if (group <= 4) return Smem<KV, D, BS, 4, NS, W>::kBytes;
+  return Smem<KV, D, BS, 8, NS, W>::kBytes;
 }
 
-template <int KV>
+template <int KV, bool TC>
 size_t smem_bytes_kv(int D, int BS, int group) {
-  if (D == 64 && BS == 16) return smem_bytes_g<KV, 64, 16>(group);
-  if (D == 64 && BS == 32) return smem_bytes_g<KV, 64, 32>(group);
-  if (D == 128 && BS == 16) return smem_bytes_g<KV, 128, 16>(group);
-  return smem_bytes_g<KV, 128, 32>(group);
+  if (D == 64 && BS == 16) return smem_bytes_g<KV, 64, 16, TC>(group);
+  if (D == 64 && BS == 32) return smem_bytes_g<KV, 64, 32, TC>(group);
+  if (D == 128 && BS == 16) return smem_bytes_g<KV, 128, 16, TC>(group);
+  return smem_bytes_g<KV, 128, 32, TC>(group);
 }
 
 }  // namespace
+
+bool make_pool_maps(const PoolDev& pool, PoolMaps& maps) {
+  maps.valid = 0;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  auto encode = reinterpret_cast<CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill)>(fn);
+  const unsigned long long rows =
+      (unsigned long long)pool.num_blocks * pool.num_kv_heads * pool.block_size;
+  if (rows >= (1ull << 31)) return false;  // row coordinates are int32
+  const cuuint64_t gdim[2] = {(cuuint64_t)pool.head_dim, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)pool.head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)pool.block_size};
+  const cuuint32_t estr[2] = {1, 1};
+  for (int t = 0; t < 2; ++t) {
+    CUresult r = encode(t == 0 ? &maps.k : &maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        t == 0 ? (void*)pool.k : (void*)pool.v, gdim, gstride, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  maps.valid = 1;
+  return true;
+}
 
 size_t decode_workspace_bytes(int num_ctas, int batch, int num_kv_heads, int group, int head_dim) {
   const size_t slots = (size_t)num_ctas + (size_t)batch * num_kv_heads;
@@ -787,16 +1085,18 @@ size_t decode_workspace_bytes(int num_ctas, int batch, int num_kv_heads, int gro
          align256(sizeof(float) * slots * group * head_dim);
 }
 
-int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group) {
-  size_t smem = kv_dtype == PA_KV_BF16    ? smem_bytes_kv<PA_KV_BF16>(head_dim, block_size, group)
-                : kv_dtype == PA_KV_UINT8 ? smem_bytes_kv<PA_KV_UINT8>(head_dim, block_size, group)
-                                          : smem_bytes_kv<PA_KV_UINT4>(head_dim, block_size, group);
+int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bool tensor_cores) {
+  size_t smem = kv_dtype == PA_KV_BF16
+                    ? (tensor_cores ? smem_bytes_kv<PA_KV_BF16, true>(head_dim, block_size, group)
+                                    : smem_bytes_kv<PA_KV_BF16, false>(head_dim, block_size, group))
+                : kv_dtype == PA_KV_UINT8 ? smem_bytes_kv<PA_KV_UINT8, false>(head_dim, block_size, group)
+                                          : smem_bytes_kv<PA_KV_UINT4, false>(head_dim, block_size, group);
   const size_t per_sm = 227 * 1024;
   int n = (int)(per_sm / (smem + 1024));
   return n < 1 ? 1 : (n > 4 ? 4 : n);
 }
 
-cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const void* q,
+cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& maps, const void* q,
                           const int32_t* block_table, const int32_t* seq_lens, float* out,
                           void* workspace, DecodeLaunch& L, cudaStream_t stream) {
   const size_t slots = (size_t)L.num_ctas + (size_t)L.batch * pool.num_kv_heads;
@@ -807,6 +1107,7 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const void* q,
   ws += align256(sizeof(float) * slots * L.group);
   L.part_o = reinterpret_cast<float*>(ws);
   DecodeParams prm;
+  prm.maps = maps;
   prm.pool = pool;
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_table = block_table;

@@ -8,6 +8,7 @@
 namespace pa {
 
 struct PoolDev;
+struct PoolMaps;
 
 // Geometry of the decode launch: how the (sequence, kv head, block) work
 // list is cut into partitions and where partial results go.
@@ -18,6 +19,7 @@ struct DecodeLaunch {
   int batch;
   int max_blocks;
   float scale_log2;     // softmax_scale * log2(e)
+  bool tensor_cores;    // bf16 pools: mma consumer fed by swizzled 2-D TMA
   // workspace carve-up
   int32_t* pre_pages;   // [batch + 1] prefix sums of per-sequence block counts
   float* part_o;        // [num_ctas + batch*Hkv][group][D]
@@ -33,10 +35,14 @@ cudaError_t launch_append(int kv_dtype, const PoolDev& pool, const void* k_new, 
 size_t decode_workspace_bytes(int num_ctas, int batch, int num_kv_heads, int group, int head_dim);
 
 // Thread blocks of the decode kernel that fit on one SM for this shape.
-int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group);
+int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bool tensor_cores);
+
+// Encode the TMA descriptors of a bf16 pool (false if the driver call fails
+// or the pool is too large for 32-bit row coordinates).
+bool make_pool_maps(const PoolDev& pool, PoolMaps& maps);
 
 // Carve the workspace and launch decode + combine.
-cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const void* q,
+cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& maps, const void* q,
                           const int32_t* block_table, const int32_t* seq_lens, float* out,
                           void* workspace, DecodeLaunch& L, cudaStream_t stream);
 

@@ -1,0 +1,46 @@
+"""Byte accounting for the decode roofline.
+
+Algorithmic bytes of one decode call: K and V of every valid token (codes,
+counted per token, not per page), the scale / zero-point metadata of every
+touched (block, kv head) for quantised pools, q, out, the block-table entries
+read and the sequence lengths. A physical block shared by several sequences
+(prefix cache) is counted once.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ELEM_BITS = {"bf16": 16, "uint8": 8, "uint4": 4}
+
+
+def decode_bytes(wl) -> dict:
+    bs, D, Hkv = wl.block_size, wl.head_dim, wl.num_kv_heads
+    bits = ELEM_BITS[wl.kv_dtype]
+    # valid tokens per physical block (max over the sequences that use it)
+    valid = {}
+    logical_tokens = 0
+    for b in range(wl.batch):
+        n = int(wl.seq_lens[b])
+        logical_tokens += n
+        for lp in range(-(-n // bs)):
+            phys = int(wl.block_table[b, lp])
+            v = min(bs, n - lp * bs)
+            if valid.get(phys, 0) < v:
+                valid[phys] = v
+    unique_tokens = sum(valid.values())
+    per_token = 2 * Hkv * D * bits // 8  # K and V, all kv heads
+    meta_per_block = 0 if wl.kv_dtype == "bf16" else 2 * Hkv * D * 8  # f32 scale + i32 zp, K and V
+    pages = sum(-(-int(s) // bs) for s in wl.seq_lens)
+    q = wl.batch * wl.num_q_heads * D * 2
+    out = wl.batch * wl.num_q_heads * D * 4
+    tables = pages * 4 + wl.batch * 4
+    kv_unique = unique_tokens * per_token + len(valid) * meta_per_block
+    kv_logical = logical_tokens * per_token + pages * meta_per_block
+    return {
+        "algorithmic": kv_unique + q + out + tables,
+        "logical": kv_logical + q + out + tables,
+        "kv_unique": kv_unique,
+        "tokens_scanned": logical_tokens,
+        "unique_blocks": len(valid),
+        "pages": pages,
+    }

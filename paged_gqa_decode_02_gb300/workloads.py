@@ -37,8 +37,9 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
     Inputs are finite by construction (normal draws)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = x.view(np.uint32)
+    # finite inputs stay below 0xFF800000 + 0x8000: no uint32 overflow
+    rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
 

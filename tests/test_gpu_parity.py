@@ -16,15 +16,20 @@ def _built():
     build.build()
 
 
+def _paths(dt):
+    return ["cuda_core", "tensor_core"] if dt == "bf16" else ["cuda_core"]
+
+
+@pytest.mark.parametrize("path", ["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("splits", [0, 1, 2, 3, 1000])
-def test_tiny_config(splits):
+def test_tiny_config(splits, path):
     wl = W.tiny()
     g, o = H.load_both(wl)
     H.assert_pools_equal(g, o)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
-    got = H.gpu_decode(g, wl, num_splits=splits)
-    H.check_attention(got, ref, f"tiny splits={splits}")
+    got = H.gpu_decode(g, wl, num_splits=splits, path=path)
+    H.check_attention(got, ref, f"tiny splits={splits} {path}")
     assert g.device_error() == (0, 0)
 
 
@@ -36,9 +41,10 @@ def test_random_small(seed, dt):
     H.assert_pools_equal(g, o)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
-    for splits in (0, 1, 5, 10 ** 4):
-        got = H.gpu_decode(g, wl, num_splits=splits)
-        H.check_attention(got, ref, f"{wl.name} {dt} splits={splits}")
+    for path in _paths(dt):
+        for splits in (0, 1, 5, 10 ** 4):
+            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
+            H.check_attention(got, ref, f"{wl.name} {dt} splits={splits} {path}")
     assert g.device_error() == (0, 0)
 
 
@@ -58,17 +64,19 @@ def test_multi_step_tail_requant(dt):
         assert o.append_call(step) == 0
         H.assert_pools_equal(g, o)
         ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
-        H.check_attention(H.gpu_decode(g, wl), ref, f"steps {dt}")
+        for path in _paths(dt):
+            H.check_attention(H.gpu_decode(g, wl, path=path), ref, f"steps {dt} {path}")
 
 
 def test_empty_and_single_token_sequences():
     wl = W.make_case("edge", 41, 5, 12, 4, 64, 16, "bf16", [0, 1, 16, 0, 17], extra_blocks=2)
     g, o = H.load_both(wl, leave_last=False)
     ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
-    for splits in (0, 1, 7):
-        got = H.gpu_decode(g, wl, num_splits=splits)
-        H.check_attention(got, ref, f"edge splits={splits}")
-        assert np.all(got.reshape(5, 12, 64)[[0, 3]] == 0)
+    for path in _paths("bf16"):
+        for splits in (0, 1, 7):
+            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
+            H.check_attention(got, ref, f"edge splits={splits} {path}")
+            assert np.all(got.reshape(5, 12, 64)[[0, 3]] == 0)
 
 
 def test_bad_table_entry_sets_error_word_and_gpu_stays_usable():
@@ -122,8 +130,26 @@ def test_full_size_config(name):
     rows = H.sample_rows(wl)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
     assert st == 0
-    for splits in (0, 97):
-        got = H.gpu_decode(g, wl, num_splits=splits)
-        H.check_attention(got[rows], ref, f"{name} splits={splits}")
-        assert np.isfinite(got).all()
+    for path in _paths(wl.kv_dtype):
+        for splits in (0, 97):
+            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
+            H.check_attention(got[rows], ref, f"{name} splits={splits} {path}")
+            assert np.isfinite(got).all()
+    assert g.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "uint8"])
+def test_slices_longer_than_a_window(dt):
+    """One or two slices over thousands of pages: a thread block walks its
+    slice in several windows and runs continue across window boundaries."""
+    wl = W.make_case("long_slices", 55, 3, 8, 2, 64, 16, dt, [21000, 5, 9000], extra_blocks=1,
+                     channel_offset_sigma=0.5 if dt != "bf16" else None)
+    g, o = H.load_both(wl)
+    H.assert_pools_equal(g, o)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    for path in _paths(dt):
+        for splits in (1, 2, 3):
+            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
+            H.check_attention(got, ref, f"long slices {dt} splits={splits} {path}")
     assert g.device_error() == (0, 0)
