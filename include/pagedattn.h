@@ -149,6 +149,27 @@ PA_API pa_status pa_decode(pa_pool* pool, const void* q, const int32_t* block_ta
                     int32_t max_blocks, float softmax_scale, float* out, void* workspace,
                     size_t workspace_bytes, int32_t num_splits, void* stream);
 
+/* pa_decode_noalloc: pa_decode for callers that cannot allocate device
+ * memory (no allocator on the hot path, memory reserved up front, or no
+ * allocator to hand a workspace from). The pages this library follows have no
+ * counterpart of it. It computes exactly what pa_decode computes, with the
+ * split-KV scratch taken from a fixed 8 MiB array in the library's device
+ * image instead of a caller workspace; it calls no allocating routine.
+ *   - The array exists on every device that loads the library, until the
+ *     process exits. The first call on a device looks up the array's device
+ *     address (with the pool's device current); make that first call before
+ *     any stream capture.
+ *   - Batches whose scratch need (pa_decode_workspace_bytes) exceeds 8 MiB are
+ *     rejected with PA_ERR_OOM and a message naming both sizes.
+ *   - All calls on a device share the one array and nothing in it must start
+ *     at zero: calls whose GPU work overlaps (other streams, other host
+ *     threads) race on it; serialise them.
+ * Other arguments, errors and semantics as pa_decode. */
+PA_API pa_status pa_decode_noalloc(pa_pool* pool, const void* q, const int32_t* block_table,
+                                   const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                   int32_t max_blocks, float softmax_scale, float* out,
+                                   int32_t num_splits, void* stream);
+
 /* Bytes of workspace pa_decode needs for this batch, head count and split
  * count (0 = the automatic split count); 0 on invalid arguments. */
 PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int32_t num_q_heads,

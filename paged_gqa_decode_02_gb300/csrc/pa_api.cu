@@ -3,6 +3,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "pa_common.cuh"
@@ -295,3 +296,60 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ decode without allocation
+//
+// Some callers cannot call cudaMalloc at all: code running under an allocator
+// that forbids device allocations on the hot path, processes whose memory is
+// reserved up front, or callers that have no allocator handle to give us.
+// pa_decode_noalloc serves them: its split-KV scratch is a fixed array in
+// this library's device image (allocated once, when the library's module is
+// loaded on a device, and held until the process exits), so a call needs no
+// workspace from the caller and allocates nothing.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+extern "C" pa_status pa_decode_noalloc(pa_pool* p, const void* q, const int32_t* block_table,
+                                       const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_blocks, float softmax_scale, float* out,
+                                       int32_t num_splits, void* stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  const int dev = p->desc.device;
+  if (dev >= kNoAllocMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device ordinal above 63%s");
+  const size_t need = pa_decode_workspace_bytes(p, batch, num_q_heads, num_splits);
+  if (batch > 0 && need == 0) return fail(PA_ERR_INVALID_ARG, "invalid batch, head count or split count%s");
+  if (need > kNoAllocScratchBytes) {
+    snprintf(g_last_error, sizeof g_last_error,
+             "pa_decode_noalloc: this batch needs %zu bytes of split-KV scratch but the static "
+             "scratch holds %zu; use pa_decode with a caller workspace or fewer splits",
+             need, kNoAllocScratchBytes);
+    return PA_ERR_OOM;
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    scratch = g_noalloc_ptr[dev];
+    if (!scratch) {
+      // first call on this device: look up the array's device address with the
+      // pool's device current (the host-side name is not a device address)
+      DeviceGuard dg(dev);
+      if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+      cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+      if (e != cudaSuccess || !scratch) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+      g_noalloc_ptr[dev] = scratch;
+    }
+  }
+  return pa_decode(p, q, block_table, seq_lens, batch, num_q_heads, max_blocks, softmax_scale, out,
+                   scratch, kNoAllocScratchBytes, num_splits, stream);
+}
