@@ -141,6 +141,7 @@ def run_ours(args):
     wl = W.CONFIGS[args.workload]()
     dev = torch.device("cuda", local)
     pool = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, local)
+    pool.set_decode_path(args.path, fused_combine=(args.combine == "fused"))
 
     def d(a):
         a = np.ascontiguousarray(a)
@@ -255,7 +256,9 @@ def run_ours(args):
                    "num_q_heads": Hq, "num_kv_heads": wl.num_kv_heads, "head_dim": D,
                    "block_size": wl.block_size, "kv_dtype": wl.kv_dtype,
                    "tokens_cached": nb["tokens_scanned"], "num_splits": splits_used,
-                   "step": "append 1 token/seq (kv_quant_append) + paged_gqa_decode + combine",
+                   "step": "append 1 token/seq (kv_quant_append) + paged_gqa_decode (split-KV merge: "
+                           + args.combine + ")",
+                   "decode_path": args.path,
                    "l2": "flushed before every timed step (256 MiB write, outside the event brackets)",
                    "parallelism": f"replicas x{world} (no exchange)"},
         "hbm_gbs": achieved,
@@ -359,6 +362,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen25_7b_bf16", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core"])
+    ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
     ap.add_argument("--cpu-seqs", type=int, default=1 << 30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

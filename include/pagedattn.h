@@ -135,7 +135,9 @@ PA_API pa_status pa_append_kv(pa_pool* pool, const void* k_new, const void* v_ne
  *   softmax_scale usually 1/sqrt(head_dim)
  *   out          device float32 [batch][num_q_heads][head_dim]
  *   workspace    device scratch of at least pa_decode_workspace_bytes(...)
- *                bytes (256-byte aligned), caller-owned; not read before written
+ *                bytes (256-byte aligned), caller-owned. Zero it once after
+ *                allocating it: a small part holds merge tickets tagged with
+ *                the call that wrote them; nothing else is read before written
  *   num_splits   number of equal partitions of the (sequence, kv head, block)
  *                work list, one thread block each (0 = one per resident slot
  *                of the device). Sequences cut by a partition boundary are
@@ -182,9 +184,17 @@ PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
  * it is built (bf16 pools: scores and P.V as mma.m16n8k16 over the GQA group,
  * pages staged by swizzled 2-D TMA) and the CUDA-core kernel otherwise;
  * CUDA_CORE forces the fp32 FMA kernel (kept for comparison). Both compute
- * the same operation. PA_ERR_UNSUPPORTED if TENSOR_CORE is asked for a pool
- * it does not serve. */
-typedef enum { PA_DECODE_AUTO = 0, PA_DECODE_CUDA_CORE = 1, PA_DECODE_TENSOR_CORE = 2 } pa_decode_path;
+ * the same operation. Sequences cut by slice boundaries are merged by a
+ * separate log-sum-exp combine kernel; OR-ing PA_DECODE_FUSED_COMBINE merges
+ * them inside the decode kernel instead (the last slice to finish a sequence
+ * merges its partials, found through call-tagged tickets).
+ * PA_ERR_UNSUPPORTED if TENSOR_CORE is asked for a pool it does not serve. */
+typedef enum {
+  PA_DECODE_AUTO = 0,
+  PA_DECODE_CUDA_CORE = 1,
+  PA_DECODE_TENSOR_CORE = 2,
+  PA_DECODE_FUSED_COMBINE = 4
+} pa_decode_path;
 PA_API pa_status pa_pool_set_decode_path(pa_pool* pool, int32_t path);
 
 /* Device addresses of the pool's arrays, for inspection and tests. */

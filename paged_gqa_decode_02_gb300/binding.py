@@ -137,6 +137,7 @@ def pa_decode_workspace_bytes(handle, batch, num_q_heads, num_splits=0):
 
 
 PA_DECODE_AUTO, PA_DECODE_CUDA_CORE, PA_DECODE_TENSOR_CORE = 0, 1, 2
+PA_DECODE_FUSED_COMBINE = 4
 DECODE_PATHS = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
 
 
@@ -210,9 +211,12 @@ class PagedKVPool:
         pa_append_kv(self.handle, k_new, v_new, cu_new, ctx_lens, block_table, B,
                      int(block_table.shape[1]) if B else 0, max_new_per_seq, stream)
 
-    def set_decode_path(self, path):
-        """'auto', 'cuda_core' or 'tensor_core' (see pa_pool_set_decode_path)."""
-        pa_pool_set_decode_path(self.handle, path)
+    def set_decode_path(self, path, fused_combine=False):
+        """'auto', 'cuda_core' or 'tensor_core'; split sequences are merged by
+        the separate combine kernel, or inside the decode kernel with
+        fused_combine (see pa_pool_set_decode_path)."""
+        code = DECODE_PATHS[path] if isinstance(path, str) else int(path)
+        pa_pool_set_decode_path(self.handle, code | (PA_DECODE_FUSED_COMBINE if fused_combine else 0))
 
     def workspace_bytes(self, batch, num_q_heads, num_splits=0):
         return pa_decode_workspace_bytes(self.handle, batch, num_q_heads, num_splits)
@@ -223,7 +227,8 @@ class PagedKVPool:
     def workspace(self, batch, num_q_heads, num_splits=0):
         n = self.workspace_bytes(batch, num_q_heads, num_splits)
         if self._ws is None or self._ws.numel() < n:
-            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+            # zeroed once: part of it holds call-tagged merge tickets
+            self._ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws
 
     def decode(self, q, block_table, seq_lens, softmax_scale, out=None, workspace=None, num_splits=0,

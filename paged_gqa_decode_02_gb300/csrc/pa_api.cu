@@ -3,6 +3,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -14,6 +15,7 @@ struct pa_pool {
   pa::PoolMaps maps;  // first: 64-byte aligned member
   pa_pool_desc desc;
   int32_t decode_path;
+  bool fused_combine;
   void* slab;
   size_t slab_bytes;
   pa::PoolDev dev;
@@ -25,6 +27,15 @@ struct pa_pool {
 namespace {
 
 thread_local char g_last_error[512] = "";
+
+// Tags of decode calls: the split-KV merge tickets in the workspace carry the
+// tag of the call that wrote them, so stale tickets never need clearing.
+std::atomic<unsigned long long> g_epoch{0};
+
+unsigned long long next_epoch() {
+  unsigned long long e = (g_epoch.fetch_add(1) + 1) & ((1ull << 40) - 1);
+  return e ? e : next_epoch();
+}
 
 pa_status fail(pa_status s, const char* fmt, const char* detail = "") {
   snprintf(g_last_error, sizeof g_last_error, fmt, detail);
@@ -159,6 +170,7 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
     return cuda_fail(e, "pool initialisation");
   }
   p->decode_path = PA_DECODE_AUTO;
+  p->fused_combine = false;
   p->maps.valid = 0;
   if (d->kv_dtype == PA_KV_BF16) pa::make_pool_maps(p->dev, p->maps);
   *out = p;
@@ -234,11 +246,13 @@ pa_status pa_append_kv(pa_pool* p, const void* k_new, const void* v_new, const i
 pa_status pa_pool_set_decode_path(pa_pool* p, int32_t path) {
   g_last_error[0] = 0;
   if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
-  if (path < PA_DECODE_AUTO || path > PA_DECODE_TENSOR_CORE)
+  const int kernel = path & 3;
+  if (path < 0 || (path & ~(3 | PA_DECODE_FUSED_COMBINE)) || kernel > PA_DECODE_TENSOR_CORE)
     return fail(PA_ERR_INVALID_ARG, "unknown decode path%s");
-  if (path == PA_DECODE_TENSOR_CORE && !(p->desc.kv_dtype == PA_KV_BF16 && p->maps.valid))
+  if (kernel == PA_DECODE_TENSOR_CORE && !(p->desc.kv_dtype == PA_KV_BF16 && p->maps.valid))
     return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path needs a bf16 pool%s");
-  p->decode_path = path;
+  p->decode_path = kernel;
+  p->fused_combine = (path & PA_DECODE_FUSED_COMBINE) != 0;
   return PA_OK;
 }
 
@@ -289,6 +303,8 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   L.max_blocks = max_blocks;
   L.scale_log2 = softmax_scale * 1.4426950408889634f;
   L.tensor_cores = uses_tensor_cores(p);
+  L.fused_combine = p->fused_combine;
+  L.epoch = next_epoch();
   cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
                                     workspace, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode launch");

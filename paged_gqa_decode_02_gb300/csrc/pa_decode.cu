@@ -40,11 +40,12 @@ namespace pa {
 
 namespace {
 
-// Consumer warps per thread block: the tensor-core consumer is short but
-// latency-bound, so it runs twice as many warps to keep each scheduler busy.
+// Consumer warps per thread block. Four tensor-core warps (one per
+// scheduler) keep up with HBM, so shared memory goes to the page ring; the
+// CUDA-core consumer is issue-bound and runs eight.
 template <bool TC>
 constexpr int consumer_warps() {
-  return TC ? 8 : 4;
+  return TC ? 4 : 8;
 }
 constexpr int kMaxSegs = 64;         // segments per window
 constexpr int kMaxWinPages = 1024;   // pages per window (block-table entries staged in smem)
@@ -108,12 +109,98 @@ struct DecodeParams {
   int32_t* pre_pages;
   float* part_o;
   float* part_lse;
+  unsigned long long* tickets;  // per unit: (epoch << 24) | slices finished
+  unsigned long long epoch;     // 40-bit call tag, never 0
+  int fused;                    // merge split units in this kernel (else: combine kernel)
   int batch;
   int num_q_heads;
   int group;
   int max_blocks;
   float scale_log2;
 };
+
+// ------------------------------------------------------------------ split-KV merge
+//
+// A unit cut by slice boundaries leaves one partial (o = acc / l,
+// lse = m + log2 l) per slice. Merging them is the online-softmax update
+// applied to whole states: M = max_s lse_s, w_s = 2^(lse_s - M),
+// out = sum_s w_s o_s / sum_s w_s. Slice i holds a partial of the unit (in
+// slot i + u) iff its page range meets the unit's; slices between the first
+// and last owner can be empty when there are more slices than pages.
+struct UnitSlices {
+  long long first, last, us, n, T, G;
+  __device__ __forceinline__ bool has_part(long long i) const {
+    const long long a = T * i / G, z = T * (i + 1) / G;
+    return (a > us ? a : us) < (z < us + n ? z : us + n);
+  }
+  __device__ __forceinline__ int count() const {
+    int c = 0;
+    for (long long i = first; i <= last; ++i) c += has_part(i);
+    return c;
+  }
+};
+
+// Merge the partials of unit u into out rows row0 .. row0+group-1, by threads
+// tid = 0..nthr-1 (all of them call; `sync` synchronises exactly them).
+// wgt: shared scratch of 32 x 8 + 8 floats. Partials are read through L2
+// (written by other thread blocks of this launch).
+template <int D, typename Sync>
+__device__ __forceinline__ void merge_unit_partials(const UnitSlices& us, long long u, long long row0,
+                                                    int group, const float* part_o,
+                                                    const float* part_lse, float* out, int tid,
+                                                    int nthr, float* wgt, Sync sync) {
+  constexpr int kMaxSl = 32;
+  float* inv_tot = wgt + kMaxSl * 8;
+  const long long nsl = us.last - us.first + 1;
+  if (nsl <= kMaxSl) {
+    for (int i = tid; i < nsl * group; i += nthr) {
+      const int sl = i / group, h = i % group;
+      wgt[sl * 8 + h] = us.has_part(us.first + sl) ? __ldcg(part_lse + (us.first + sl + u) * group + h)
+                                                   : -INFINITY;
+    }
+    sync();
+    if (tid < group) {
+      float M = -INFINITY;
+      for (int sl = 0; sl < nsl; ++sl) M = fmaxf(M, wgt[sl * 8 + tid]);
+      float W = 0.0f;
+      for (int sl = 0; sl < nsl; ++sl) {
+        const float w = wgt[sl * 8 + tid] == -INFINITY ? 0.0f : exp2f(wgt[sl * 8 + tid] - M);
+        wgt[sl * 8 + tid] = w;
+        W += w;
+      }
+      inv_tot[tid] = W > 0.0f ? 1.0f / W : 0.0f;
+    }
+    sync();
+    for (int e = tid; e < group * D; e += nthr) {
+      const int h = e / D;
+      float A = 0.0f;
+#pragma unroll 4
+      for (int sl = 0; sl < nsl; ++sl) {
+        const float w = wgt[sl * 8 + h];
+        if (w != 0.0f) A += w * __ldcg(part_o + (us.first + sl + u) * group * D + e);
+      }
+      out[row0 * D + e] = A * inv_tot[h];
+    }
+    sync();
+    return;
+  }
+  for (int e = tid; e < group * D; e += nthr) {
+    const int h = e / D;
+    float M = -INFINITY;
+    for (long long i = us.first; i <= us.last; ++i)
+      if (us.has_part(i)) M = fmaxf(M, __ldcg(part_lse + (i + u) * group + h));
+    float W = 0.0f, A = 0.0f;
+    for (long long i = us.first; i <= us.last; ++i) {
+      if (!us.has_part(i)) continue;
+      const float l = __ldcg(part_lse + (i + u) * group + h);
+      const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
+      W += w;
+      A += w * __ldcg(part_o + (i + u) * group * D + e);
+    }
+    out[row0 * D + e] = W > 0.0f ? A / W : 0.0f;
+  }
+  sync();
+}
 
 // Sequence length clamped to what the table can hold; bad lengths count as 0.
 __device__ __forceinline__ int seq_len_checked(const DecodeParams& p, int b, bool report) {
@@ -544,6 +631,7 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
   __shared__ volatile int abort_flag;
   __shared__ int issued_n[NST];  // last fill issued per stage (drain on abort)
   __shared__ int q_issued[2];    // last q segment index issued per slot
+  __shared__ int merge_flag;
 
   // Launched with programmatic stream serialization: let the combine kernel
   // be scheduled early, but touch no global memory before the preceding
@@ -566,11 +654,20 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
     fence_mbar_init();
   }
 
-  // ---- plan: total pages, this slice, and where it starts
+  // ---- plan: total pages, this slice, and where it starts. Checked lengths
+  // of the first kLensSmem sequences are kept in shared memory (in the merge
+  // stash, idle until the first merge) for the second pass and the first
+  // window's segment list.
+  int* lens_sm = reinterpret_cast<int*>(stash_acc);
+  constexpr int kLensSmem = (int)(SM::kStashAccBytes / 4);
   long long npages_all = 0;
   {
     int part = 0;
-    for (int b = tid; b < p.batch; b += kThreads) part += (seq_len_checked(p, b, cta == 0) + BS - 1) / BS;
+    for (int b = tid; b < p.batch; b += kThreads) {
+      const int len = seq_len_checked(p, b, cta == 0);
+      if (b < kLensSmem) lens_sm[b] = len;
+      part += (len + BS - 1) / BS;
+    }
     int tot;
     block_incl_scan(part, warp_tot, tot);
     npages_all = tot;
@@ -584,7 +681,7 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
     int running = 0;
     for (int base = 0; base < p.batch; base += kThreads) {
       const int b = base + tid;
-      const int n = b < p.batch ? (seq_len_checked(p, b, false) + BS - 1) / BS : 0;
+      const int n = b < p.batch ? ((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS : 0;
       int tot;
       const int incl = block_incl_scan(n, warp_tot, tot);
       const long long lo = (long long)(running + incl - n) * Hkv;
@@ -606,6 +703,15 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
       }
     }
     if (cta == 0 && p.batch == 0 && tid == 0) p.pre_pages[0] = 0;
+    if (cta == 0 && p.fused) {
+      // rows of empty sequences: no slice holds a page of them
+      const int row_elems = p.num_q_heads * D;
+      for (int b = 0; b < p.batch; ++b) {
+        const int len = b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false);
+        if (len == 0)
+          for (int e = tid; e < row_elems; e += kThreads) p.out[(long long)b * row_elems + e] = 0.0f;
+      }
+    }
   }
   __syncthreads();
   if (s_i >= e_i) return;  // no pages for this thread block
@@ -613,6 +719,7 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
   long long cur_b = plan[0], cur_base = plan[1];  // sequence holding `pos` and its first page
   long long pos = s_i;
   int seg_counter = 0;      // segments started so far (q slot ring index)
+  bool lens_cached = true;  // lens_sm valid until the first merge overwrites the stash
   uint64_t pol = policy_evict_first();
   Cons cons;  // consumer warps' online-softmax state; persists across windows
 
@@ -625,7 +732,9 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
       bool done = false;
       while (!done && b0 < p.batch) {
         const long long bb = b0 + lane;
-        const int len = bb < p.batch ? seq_len_checked(p, (int)bb, false) : 0;
+        const int len = bb >= p.batch ? 0
+                        : (lens_cached && bb < kLensSmem) ? lens_sm[bb]
+                                                          : seq_len_checked(p, (int)bb, false);
         const int n = (len + BS - 1) / BS;
         int x = n;
 #pragma unroll
@@ -857,10 +966,45 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
             if (c == 0) p.part_lse[(long long)sg.slot * g + h] = Lsum > 0.0f ? M + log2f(Lsum) : -INFINITY;
           }
         }
+        if (sg.slot >= 0 && p.fused) {
+          // the last slice to finish this unit merges its partials (threadfence
+          // reduction: partials are fenced before the ticket is taken)
+          __threadfence();
+          named_bar_sync(1, kConsumerWarps * 32);
+          UnitSlices usl;
+          usl.n = (sg.len + BS - 1) / BS;
+          usl.us = s_i + sg.k0 - sg.lp0;
+          usl.T = T;
+          usl.G = Gc;
+          usl.first = owner_of(usl.us, T, Gc);
+          usl.last = owner_of(usl.us + usl.n - 1, T, Gc);
+          const long long u = (long long)sg.b * Hkv + sg.h;
+          if (ctid == 0) {
+            const unsigned long long tag = p.epoch << 24;
+            unsigned long long* t = p.tickets + u;
+            unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(t), assumed;
+            unsigned long long mine;
+            do {
+              assumed = old;
+              const unsigned long long done = (assumed >> 24) == p.epoch ? (assumed & 0xFFFFFFull) : 0ull;
+              mine = done + 1;
+              old = atomicCAS(t, assumed, tag | mine);
+            } while (old != assumed);
+            merge_flag = mine == (unsigned long long)usl.count() ? 1 : 0;
+          }
+          named_bar_sync(1, kConsumerWarps * 32);
+          if (merge_flag) {
+            __threadfence();
+            merge_unit_partials<D>(usl, u, row0, g, p.part_o, p.part_lse, p.out, ctid,
+                                   kConsumerWarps * 32, stash_acc,
+                                   [] { named_bar_sync(1, kConsumerWarps * 32); });
+          }
+        }
         named_bar_sync(1, kConsumerWarps * 32);
       }
     }
     seg_counter += nseg;
+    lens_cached = false;
     pos = wend;
     __syncthreads();
   }
@@ -886,9 +1030,7 @@ __global__ void __launch_bounds__(256)
     splitkv_combine_kernel(const int32_t* pre_pages, const float* part_o, const float* part_lse,
                            float* out, int batch, int num_kv_heads, int group, int num_q_heads,
                            int num_ctas) {
-  constexpr int kMaxSl = 32;
-  __shared__ float wgt[kMaxSl][8];
-  __shared__ float inv_tot[8];
+  __shared__ float wgt[32 * 8 + 8];
   pdl_launch_dependents();
   pdl_wait();
   const int u = blockIdx.x, tid = threadIdx.x;
@@ -901,63 +1043,16 @@ __global__ void __launch_bounds__(256)
     for (int e = tid; e < group * D; e += blockDim.x) out[row0 * D + e] = 0.0f;
     return;
   }
-  const long long us = pre * num_kv_heads + (long long)j * n;
-  const long long first = owner_of(us, T, num_ctas), last = owner_of(us + n - 1, T, num_ctas);
-  if (first == last) return;
-  // slice i holds a partial of this unit (in slot i + u) iff its page range
-  // meets the unit's; slices between first and last can be empty when there
-  // are more slices than pages
-  auto has_part = [&](long long i) {
-    const long long a = T * i / num_ctas, z = T * (i + 1) / num_ctas;
-    return (a > us ? a : us) < (z < us + n ? z : us + n);
-  };
-  const long long nsl = last - first + 1;
-  if (nsl <= kMaxSl) {
-    if (tid < nsl * group) {
-      const int sl = tid / group, h = tid % group;
-      wgt[sl][h] = has_part(first + sl) ? part_lse[(first + sl + u) * group + h] : -INFINITY;
-    }
-    __syncthreads();
-    if (tid < group) {
-      float M = -INFINITY;
-      for (int sl = 0; sl < nsl; ++sl) M = fmaxf(M, wgt[sl][tid]);
-      float W = 0.0f;
-      for (int sl = 0; sl < nsl; ++sl) {
-        const float w = wgt[sl][tid] == -INFINITY ? 0.0f : exp2f(wgt[sl][tid] - M);
-        wgt[sl][tid] = w;
-        W += w;
-      }
-      inv_tot[tid] = W > 0.0f ? 1.0f / W : 0.0f;
-    }
-    __syncthreads();
-    for (int e = tid; e < group * D; e += blockDim.x) {
-      const int h = e / D;
-      float A = 0.0f;
-#pragma unroll 4
-      for (int sl = 0; sl < nsl; ++sl) {
-        const float w = wgt[sl][h];
-        if (w != 0.0f) A += w * part_o[(first + sl + u) * group * D + e];
-      }
-      out[row0 * D + e] = A * inv_tot[h];
-    }
-    return;
-  }
-  // many slices (forced large split counts): straightforward two-pass merge
-  for (int e = tid; e < group * D; e += blockDim.x) {
-    const int h = e / D;
-    float M = -INFINITY;
-    for (long long i = first; i <= last; ++i)
-      if (has_part(i)) M = fmaxf(M, part_lse[(i + u) * group + h]);
-    float W = 0.0f, A = 0.0f;
-    for (long long i = first; i <= last; ++i) {
-      if (!has_part(i)) continue;
-      const float l = part_lse[(i + u) * group + h];
-      const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
-      W += w;
-      A += w * part_o[(i + u) * group * D + e];
-    }
-    out[row0 * D + e] = W > 0.0f ? A / W : 0.0f;
-  }
+  UnitSlices usl;
+  usl.us = pre * num_kv_heads + (long long)j * n;
+  usl.n = n;
+  usl.T = T;
+  usl.G = num_ctas;
+  usl.first = owner_of(usl.us, T, num_ctas);
+  usl.last = owner_of(usl.us + n - 1, T, num_ctas);
+  if (usl.first == usl.last) return;
+  merge_unit_partials<D>(usl, u, row0, group, part_o, part_lse, out, tid, blockDim.x, wgt,
+                         [] { __syncthreads(); });
 }
 
 template <int KV, int D, int BS, int G, int NS, bool TC>
@@ -983,7 +1078,7 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return e;
   const int units = prm.batch * prm.pool.num_kv_heads;
-  if (units == 0) return cudaSuccess;
+  if (units == 0 || prm.fused) return cudaSuccess;
   cfg.gridDim = dim3(units);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
@@ -993,12 +1088,24 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
                             L.num_ctas);
 }
 
-// Stages per consumer warp: as many pages in flight as fit a ~160 KB ring
-// (1..4 per warp; one only for 16 KB pages with eight consumer warps).
+// Stages per consumer warp: as many pages in flight as the shared memory
+// allows next to the fixed parts (1..8 per warp, largest that fits with 1 KB
+// of static shared memory to spare). Bytes in flight per SM are what sustains
+// HBM bandwidth (Little's law), so the ring gets the rest.
+template <int KV, int D, int BS, int W, int N>
+constexpr int largest_ring() {
+  if constexpr (N <= 1) {
+    return 1;
+  } else if constexpr (Smem<KV, D, BS, 8, N, W>::kBytes + 1024 <= 227 * 1024) {
+    return N;
+  } else {
+    return largest_ring<KV, D, BS, W, N - 1>();
+  }
+}
+
 template <int KV, int D, int BS, int W>
 constexpr int stages_per_warp() {
-  constexpr int n = (160 * 1024) / (W * PageGeom<KV, D, BS>::kStageBytes);
-  return n < 1 ? 1 : (n > 4 ? 4 : n);
+  return largest_ring<KV, D, BS, W, 8>();
 }
 
 template <int KV, int D, int BS, bool TC>
@@ -1081,7 +1188,8 @@ bool make_pool_maps(const PoolDev& pool, PoolMaps& maps) {
 
 size_t decode_workspace_bytes(int num_ctas, int batch, int num_kv_heads, int group, int head_dim) {
   const size_t slots = (size_t)num_ctas + (size_t)batch * num_kv_heads;
-  return align256(sizeof(int32_t) * ((size_t)batch + 1)) + align256(sizeof(float) * slots * group) +
+  return align256(sizeof(unsigned long long) * (size_t)batch * num_kv_heads) +
+         align256(sizeof(int32_t) * ((size_t)batch + 1)) + align256(sizeof(float) * slots * group) +
          align256(sizeof(float) * slots * group * head_dim);
 }
 
@@ -1101,6 +1209,8 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& map
                           void* workspace, DecodeLaunch& L, cudaStream_t stream) {
   const size_t slots = (size_t)L.num_ctas + (size_t)L.batch * pool.num_kv_heads;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+  ws += align256(sizeof(unsigned long long) * (size_t)L.batch * pool.num_kv_heads);
   L.pre_pages = reinterpret_cast<int32_t*>(ws);
   ws += align256(sizeof(int32_t) * ((size_t)L.batch + 1));
   L.part_lse = reinterpret_cast<float*>(ws);
@@ -1116,6 +1226,9 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& map
   prm.pre_pages = L.pre_pages;
   prm.part_o = L.part_o;
   prm.part_lse = L.part_lse;
+  prm.tickets = tickets;
+  prm.epoch = L.epoch;
+  prm.fused = L.fused_combine ? 1 : 0;
   prm.batch = L.batch;
   prm.num_q_heads = L.num_q_heads;
   prm.group = L.group;

@@ -20,16 +20,17 @@ def _paths(dt):
     return ["cuda_core", "tensor_core"] if dt == "bf16" else ["cuda_core"]
 
 
+@pytest.mark.parametrize("combine", ["fused", "separate"])
 @pytest.mark.parametrize("path", ["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("splits", [0, 1, 2, 3, 1000])
-def test_tiny_config(splits, path):
+def test_tiny_config(splits, path, combine):
     wl = W.tiny()
     g, o = H.load_both(wl)
     H.assert_pools_equal(g, o)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
-    got = H.gpu_decode(g, wl, num_splits=splits, path=path)
-    H.check_attention(got, ref, f"tiny splits={splits} {path}")
+    got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
+    H.check_attention(got, ref, f"tiny splits={splits} {path} {combine}")
     assert g.device_error() == (0, 0)
 
 
@@ -43,8 +44,9 @@ def test_random_small(seed, dt):
     assert st == 0
     for path in _paths(dt):
         for splits in (0, 1, 5, 10 ** 4):
-            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
-            H.check_attention(got, ref, f"{wl.name} {dt} splits={splits} {path}")
+            for combine in ("fused", "separate"):
+                got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
+                H.check_attention(got, ref, f"{wl.name} {dt} splits={splits} {path} {combine}")
     assert g.device_error() == (0, 0)
 
 
@@ -74,9 +76,10 @@ def test_empty_and_single_token_sequences():
     ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     for path in _paths("bf16"):
         for splits in (0, 1, 7):
-            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
-            H.check_attention(got, ref, f"edge splits={splits} {path}")
-            assert np.all(got.reshape(5, 12, 64)[[0, 3]] == 0)
+            for combine in ("fused", "separate"):
+                got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
+                H.check_attention(got, ref, f"edge splits={splits} {path} {combine}")
+                assert np.all(got.reshape(5, 12, 64)[[0, 3]] == 0)
 
 
 def test_bad_table_entry_sets_error_word_and_gpu_stays_usable():
@@ -131,9 +134,9 @@ def test_full_size_config(name):
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
     assert st == 0
     for path in _paths(wl.kv_dtype):
-        for splits in (0, 97):
-            got = H.gpu_decode(g, wl, num_splits=splits, path=path)
-            H.check_attention(got[rows], ref, f"{name} splits={splits} {path}")
+        for splits, combine in ((0, "fused"), (97, "fused"), (0, "separate")):
+            got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
+            H.check_attention(got[rows], ref, f"{name} splits={splits} {path} {combine}")
             assert np.isfinite(got).all()
     assert g.device_error() == (0, 0)
 
@@ -152,4 +155,20 @@ def test_slices_longer_than_a_window(dt):
         for splits in (1, 2, 3):
             got = H.gpu_decode(g, wl, num_splits=splits, path=path)
             H.check_attention(got, ref, f"long slices {dt} splits={splits} {path}")
+    assert g.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("combine", ["fused", "separate"])
+@pytest.mark.parametrize("splits", [0, 300, 2000])
+def test_many_slices_per_sequence(splits, combine):
+    """Units cut into many slices (up to 32 and beyond) with a 7-head group:
+    the merge stages slices x heads log-sum-exps with fewer threads than
+    entries."""
+    wl = W.make_case("many_slices", 92, 3, 28, 4, 128, 16, "bf16", [700, 33, 1500], extra_blocks=2)
+    g, o = H.load_both(wl)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    for path in _paths("bf16"):
+        got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
+        H.check_attention(got, ref, f"many slices splits={splits} {path} {combine}")
     assert g.device_error() == (0, 0)
