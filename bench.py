@@ -42,6 +42,28 @@ WORKLOAD_TEXT = {
 }
 
 
+PROFILE_FOR = {"qwen25_7b_bf16": "profiles/paged_gqa_decode_qwen25_7b_bf16.md"}
+
+
+def _traffic(workload, path):
+    """DRAM bytes per decode launch from the committed ncu summary, or None
+    when there is none for this workload or the kernel source changed since."""
+    import hashlib
+    rel = PROFILE_FOR.get(workload)
+    if rel is None or path not in ("auto", "tensor_core"):
+        return None
+    try:
+        text = open(os.path.join(ROOT, rel)).read()
+        fields = dict(l.split(": ", 1) for l in text.splitlines() if l.startswith(("traffic_", "source_")))
+        src = b"".join(open(os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc", f), "rb").read()
+                       for f in ("pa_decode.cu", "pa_common.cuh"))
+        if hashlib.sha256(src).hexdigest()[:16] != fields["source_sha256_16"].strip():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -265,7 +287,7 @@ def run_ours(args):
         "decode_us": t_dec_max * 1e6,
         "kv_tokens_per_s": world * nb["tokens_scanned"] / t_dec_max,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": _traffic(args.workload, args.path),
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": nb["algorithmic"],
