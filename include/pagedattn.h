@@ -26,14 +26,17 @@
  *    3.7.2 item 5).
  *
  * Storage format of a pool (library-owned device memory, one allocation):
- *   bf16 : K, V     bf16  [num_blocks][Hkv][block_size][head_dim]
- *   uint8: K, V     uint8 [num_blocks][Hkv][block_size][head_dim]
- *   uint4: K, V     uint8 [num_blocks][Hkv][block_size][head_dim/2],
- *                   channel 2i in the low nibble, 2i+1 in the high nibble
- *   quantised pools also hold, for K and for V, scale float32 and zero point
- *   int32 [num_blocks][Hkv][head_dim] -- one pair per (physical block, kv
- *   head, channel). Every page (one block of one kv head) starts on a 256-byte
- *   boundary.
+ * records of pages, [num_blocks][Hkv] records, a page being one block of one
+ * kv head, each record contiguous:
+ *   bf16 : K bf16 [block_size][head_dim], V bf16 [block_size][head_dim]
+ *   uint8: K codes uint8 [block_size][head_dim], V codes likewise, then
+ *          K scale float32 [head_dim], K zero point int32 [head_dim],
+ *          V scale float32 [head_dim], V zero point int32 [head_dim]
+ *   uint4: as uint8 with codes uint8 [block_size][head_dim/2], channel 2i in
+ *          the low nibble and 2i+1 in the high nibble
+ * One (scale, zero point) pair per (physical block, kv head, channel).
+ * Records start on 256-byte boundaries (record bytes: 2 x codes + 4 x 4 x
+ * head_dim for quantised pools, 2 x codes for bf16).
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
@@ -81,8 +84,9 @@ typedef struct {
   int32_t device;       /* CUDA device ordinal */
 } pa_pool_desc;
 
-/* Device addresses of a pool's arrays (layouts above). Scale and zero-point
- * pointers are NULL for a bf16 pool. */
+/* Device addresses of page 0's components (layout above); page n's
+ * component lies n * page_stride bytes further. Scale and zero-point pointers
+ * are NULL for a bf16 pool. */
 typedef struct {
   void* k;
   void* v;
@@ -90,8 +94,8 @@ typedef struct {
   int32_t* k_zp;
   float* v_scale;
   int32_t* v_zp;
-  size_t kv_bytes;   /* bytes of each of k and v */
-  size_t meta_bytes; /* bytes of each scale / zero-point array (0 for bf16) */
+  size_t page_stride; /* bytes of one page record */
+  size_t num_pages;   /* num_blocks * num_kv_heads */
 } pa_pool_buffers;
 
 /* pa_create_pool: allocate a pool (one device allocation; contents zero,
@@ -181,8 +185,9 @@ PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int3
 PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
 
 /* Decode kernel selection for a pool. AUTO uses the tensor-core kernel where
- * it is built (bf16 pools: scores and P.V as mma.m16n8k16 over the GQA group,
- * pages staged by swizzled 2-D TMA) and the CUDA-core kernel otherwise;
+ * it is built (bf16 pools, and uint8 pools of head_dim 128: scores and P.V as
+ * mma.m16n8k16 over the GQA group, pages staged by swizzled 2-D TMA) and the
+ * CUDA-core kernel otherwise;
  * CUDA_CORE forces the fp32 FMA kernel (kept for comparison). Both compute
  * the same operation. Sequences cut by slice boundaries are merged by a
  * separate log-sum-exp combine kernel; OR-ing PA_DECODE_FUSED_COMBINE merges

@@ -42,7 +42,7 @@ class pa_pool_desc(ctypes.Structure):
 class pa_pool_buffers(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("k_zp", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("v_zp", ctypes.c_void_p),
-                ("kv_bytes", ctypes.c_size_t), ("meta_bytes", ctypes.c_size_t)]
+                ("page_stride", ctypes.c_size_t), ("num_pages", ctypes.c_size_t)]
 
 
 _lib = None
@@ -192,19 +192,28 @@ class PagedKVPool:
             pass
 
     def view(self):
-        """torch tensors aliasing the pool's device arrays (see pagedattn.h)."""
+        """torch tensors aliasing the pool's components (strided views over the
+        page records, see pagedattn.h)."""
         b = pa_pool_buffers()
         _check(lib().pa_pool_view(self.handle, ctypes.byref(b)))
         P, H, bs, D = self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim
-        dev = self.device
+        stride, n = int(b.page_stride), int(b.num_pages)
+        rec = _view(b.k, (n * stride,), "|u1", self.device).view(P, H, stride)
+
+        def comp(ptr, nbytes, dtype):
+            off = int(ptr) - int(b.k)
+            return rec[:, :, off:off + nbytes].view(dtype)
+
         if self.kv_dtype == "bf16":
-            return {"k": _view(b.k, (P, H, bs, D), "<i2", dev), "v": _view(b.v, (P, H, bs, D), "<i2", dev)}
+            return {"k": comp(b.k, bs * D * 2, torch.int16).unflatten(2, (bs, D)),
+                    "v": comp(b.v, bs * D * 2, torch.int16).unflatten(2, (bs, D))}
         w = D if self.kv_dtype == "uint8" else D // 2
-        return {"k": _view(b.k, (P, H, bs, w), "|u1", dev), "v": _view(b.v, (P, H, bs, w), "|u1", dev),
-                "k_scale": _view(b.k_scale, (P, H, D), "<f4", dev),
-                "k_zp": _view(b.k_zp, (P, H, D), "<i4", dev),
-                "v_scale": _view(b.v_scale, (P, H, D), "<f4", dev),
-                "v_zp": _view(b.v_zp, (P, H, D), "<i4", dev)}
+        return {"k": comp(b.k, bs * w, torch.uint8).unflatten(2, (bs, w)),
+                "v": comp(b.v, bs * w, torch.uint8).unflatten(2, (bs, w)),
+                "k_scale": comp(b.k_scale, D * 4, torch.float32),
+                "k_zp": comp(b.k_zp, D * 4, torch.int32),
+                "v_scale": comp(b.v_scale, D * 4, torch.float32),
+                "v_zp": comp(b.v_zp, D * 4, torch.int32)}
 
     def append_kv(self, k_new, v_new, cu_new, ctx_lens, block_table, max_new_per_seq=0, stream=None):
         B = int(ctx_lens.shape[0])

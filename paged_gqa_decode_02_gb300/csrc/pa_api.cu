@@ -49,9 +49,11 @@ pa_status cuda_fail(cudaError_t e, const char* where) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-__global__ void fill_f32(float* p, size_t n, float v) {
+// value v into `per` consecutive floats of each of `pages` records `stride` floats apart
+__global__ void fill_scales(float* p, size_t pages, int per, size_t stride, float v) {
+  const size_t n = pages * per;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    p[i] = v;
+    p[(i / per) * stride + i % per] = v;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -71,7 +73,7 @@ struct DeviceGuard {
 };
 
 bool uses_tensor_cores(const pa_pool* p) {
-  return p->desc.kv_dtype == PA_KV_BF16 && p->maps.valid && p->decode_path != PA_DECODE_CUDA_CORE;
+  return p->maps.valid && p->decode_path != PA_DECODE_CUDA_CORE;
 }
 
 int auto_splits(const pa_pool* p, int group) {
@@ -114,15 +116,15 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
   const size_t pages = (size_t)d->num_blocks * d->num_kv_heads;
   const size_t elem_bits = d->kv_dtype == PA_KV_BF16 ? 16 : (d->kv_dtype == PA_KV_UINT8 ? 8 : 4);
-  const size_t page_bytes = (size_t)d->block_size * d->head_dim * elem_bits / 8;
-  const size_t kv_bytes = pages * page_bytes;
-  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : pages * d->head_dim * 4;
-  const size_t slab = 256 + 2 * align256(kv_bytes) + 4 * align256(meta_bytes);
+  const size_t codes_bytes = (size_t)d->block_size * d->head_dim * elem_bits / 8;  // one of K or V
+  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : (size_t)d->head_dim * 4;  // one of 4 arrays
+  const size_t stride = 2 * codes_bytes + 4 * meta_bytes;  // one page record
+  const size_t slab = 256 + pages * stride;
   pa_pool* p = new (std::nothrow) pa_pool();
   if (!p) return fail(PA_ERR_OOM, "host allocation failed%s");
   p->desc = *d;
-  p->kv_bytes = kv_bytes;
-  p->meta_bytes = meta_bytes;
+  p->kv_bytes = pages * codes_bytes;
+  p->meta_bytes = pages * meta_bytes;
   cudaError_t e = cudaMalloc(&p->slab, slab);
   if (e != cudaSuccess) {
     delete p;
@@ -132,23 +134,19 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   p->slab_bytes = slab;
   uint8_t* base = static_cast<uint8_t*>(p->slab);
   p->dev.err = reinterpret_cast<uint32_t*>(base);
-  uint8_t* cur = base + 256;
-  p->dev.k = cur;
-  cur += align256(kv_bytes);
-  p->dev.v = cur;
-  cur += align256(kv_bytes);
+  uint8_t* rec = base + 256;
+  p->dev.stride = (long long)stride;
+  p->dev.k = rec;
+  p->dev.v = rec + codes_bytes;
   p->dev.k_scale = nullptr;
   p->dev.k_zp = nullptr;
   p->dev.v_scale = nullptr;
   p->dev.v_zp = nullptr;
   if (meta_bytes) {
-    p->dev.k_scale = reinterpret_cast<float*>(cur);
-    cur += align256(meta_bytes);
-    p->dev.k_zp = reinterpret_cast<int32_t*>(cur);
-    cur += align256(meta_bytes);
-    p->dev.v_scale = reinterpret_cast<float*>(cur);
-    cur += align256(meta_bytes);
-    p->dev.v_zp = reinterpret_cast<int32_t*>(cur);
+    p->dev.k_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes);
+    p->dev.k_zp = reinterpret_cast<int32_t*>(rec + 2 * codes_bytes + meta_bytes);
+    p->dev.v_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes + 2 * meta_bytes);
+    p->dev.v_zp = reinterpret_cast<int32_t*>(rec + 2 * codes_bytes + 3 * meta_bytes);
   }
   p->dev.num_blocks = d->num_blocks;
   p->dev.num_kv_heads = d->num_kv_heads;
@@ -158,9 +156,10 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, d->device);
   if (e == cudaSuccess && meta_bytes) {
     // scales start at 1.0 so an untouched page dequantises to its (zero) codes
-    const size_t n = meta_bytes / 4;
-    fill_f32<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256>>>(p->dev.k_scale, n, 1.0f);
-    fill_f32<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256>>>(p->dev.v_scale, n, 1.0f);
+    const size_t n = pages * d->head_dim;
+    const unsigned grid = (unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535);
+    fill_scales<<<grid, 256>>>(p->dev.k_scale, pages, d->head_dim, stride / 4, 1.0f);
+    fill_scales<<<grid, 256>>>(p->dev.v_scale, pages, d->head_dim, stride / 4, 1.0f);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
   }
@@ -172,7 +171,7 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   p->decode_path = PA_DECODE_AUTO;
   p->fused_combine = false;
   p->maps.valid = 0;
-  if (d->kv_dtype == PA_KV_BF16) pa::make_pool_maps(p->dev, p->maps);
+  if (d->kv_dtype != PA_KV_UINT4) pa::make_pool_maps(d->kv_dtype, p->dev, p->maps);
   *out = p;
   return PA_OK;
 }
@@ -197,8 +196,8 @@ pa_status pa_pool_view(const pa_pool* p, pa_pool_buffers* out) {
   out->k_zp = p->dev.k_zp;
   out->v_scale = p->dev.v_scale;
   out->v_zp = p->dev.v_zp;
-  out->kv_bytes = p->kv_bytes;
-  out->meta_bytes = p->meta_bytes;
+  out->page_stride = (size_t)p->dev.stride;
+  out->num_pages = (size_t)p->desc.num_blocks * p->desc.num_kv_heads;
   return PA_OK;
 }
 
@@ -249,8 +248,8 @@ pa_status pa_pool_set_decode_path(pa_pool* p, int32_t path) {
   const int kernel = path & 3;
   if (path < 0 || (path & ~(3 | PA_DECODE_FUSED_COMBINE)) || kernel > PA_DECODE_TENSOR_CORE)
     return fail(PA_ERR_INVALID_ARG, "unknown decode path%s");
-  if (kernel == PA_DECODE_TENSOR_CORE && !(p->desc.kv_dtype == PA_KV_BF16 && p->maps.valid))
-    return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path needs a bf16 pool%s");
+  if (kernel == PA_DECODE_TENSOR_CORE && !p->maps.valid)
+    return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path serves bf16 pools and uint8 pools of head_dim 128%s");
   p->decode_path = kernel;
   p->fused_combine = (path & PA_DECODE_FUSED_COMBINE) != 0;
   return PA_OK;

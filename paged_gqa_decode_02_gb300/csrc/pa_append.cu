@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
     const long long row0 = (long long)c0 + first - ctx;
 
     if (KV == PA_KV_BF16) {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(codes) + page * BS * D;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(page_of(codes, page, pool.stride));
       const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
       for (int s = old_cnt; s < valid; ++s)
         dst[s * D + c] = s16[((row0 + s) * Hkv + h) * D + c];
@@ -90,10 +90,12 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
     }
 
     constexpr int L = (KV == PA_KV_UINT4) ? 15 : 255;
-    uint8_t* pc = codes + page * BS * (KV == PA_KV_UINT4 ? D / 2 : D);
+    uint8_t* pc = page_of(codes, page, pool.stride);
+    float* psc = page_of(scales, page, pool.stride);
+    int32_t* pzp = page_of(zps, page, pool.stride);
     float vals[BS];
-    const float old_scale = scales[page * D + c];
-    const int32_t old_zp = zps[page * D + c];
+    const float old_scale = psc[c];
+    const int32_t old_zp = pzp[c];
 #pragma unroll
     for (int s = 0; s < BS; ++s) {
       float x = 0.0f;
@@ -139,8 +141,8 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
         if (s < valid && (c & 1) == 0) pc[s * (D / 2) + c / 2] = (uint8_t)(code[s] | (other << 4));
       }
     }
-    scales[page * D + c] = scale;
-    zps[page * D + c] = zp;
+    psc[c] = scale;
+    pzp[c] = zp;
   }
 }
 

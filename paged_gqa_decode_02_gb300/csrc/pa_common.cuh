@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,27 +11,38 @@
 
 namespace pa {
 
-// Pool geometry and device addresses, passed by value to every kernel.
+// Pool geometry and device addresses, passed by value to every kernel. A
+// page (one block of one kv head) is one contiguous record
+// [K][V][K scale][K zp][V scale][V zp]; each pointer addresses its component
+// in page 0, and page n's component sits n * stride bytes further on.
 struct PoolDev {
-  uint8_t* k;       // codes or bf16 elements
+  uint8_t* k;       // codes or bf16 elements [bs][D] (uint4: [bs][D/2])
   uint8_t* v;
-  float* k_scale;   // [P][Hkv][D] (quantised pools)
+  float* k_scale;   // [D] (quantised pools)
   int32_t* k_zp;
   float* v_scale;
   int32_t* v_zp;
   uint32_t* err;    // device error word
+  long long stride; // bytes from one page record to the next
   int32_t num_blocks;
   int32_t num_kv_heads;
   int32_t block_size;
   int32_t head_dim;
 };
 
-// TMA descriptors of a bf16 pool's K and V arrays viewed as 2-D tensors
-// [num_blocks * Hkv * block_size rows][head_dim], boxes of 64 channels x
-// block_size rows, 128-byte swizzle.
-struct PoolMaps {  // aligned as its CUtensorMap members
-  CUtensorMap k;
-  CUtensorMap v;
+template <typename T>
+__host__ __device__ __forceinline__ T* page_of(T* base, long long page, long long stride) {
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(base) + page * stride);
+}
+
+// TMA descriptor of a pool's page records viewed as a 2-D tensor of rows,
+// 128-byte swizzle. bf16: rows of head_dim elements (2*bs rows per record, K
+// then V), boxes of 64 channels x 2*bs rows (two per record for head_dim 128).
+// uint8 (head_dim 128): rows of 128 bytes (stride/128 rows per record, codes
+// then metadata), one box per record.
+struct PoolMaps {  // aligned as its CUtensorMap member
+  CUtensorMap rec;
+  int32_t rows_per_page;
   int32_t valid;
 };
 
@@ -178,6 +190,46 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, in
       "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+}  // namespace pa
+
+namespace pa {
+
+// D = A(16x16, row) * B(16x8, col) + D, f16 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte permute: bytes of {b, a} numbered 0..3 (a) and 4..7 (b); nibble i of
+// sel picks byte i of the result.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Two bytes of w (chosen by sel, see prmt) as two exact f16 integers 0..255:
+// 0x64XX is the f16 value 1024 + XX, minus 1024.
+__device__ __forceinline__ uint32_t bytes_to_f16x2(uint32_t w, uint32_t sel) {
+  const uint32_t x = prmt(w, 0x64646464u, sel);
+  __half2 h = *reinterpret_cast<const __half2*>(&x);
+  h = __hsub2(h, __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400)));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_f16(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 }  // namespace pa

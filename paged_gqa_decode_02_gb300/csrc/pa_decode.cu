@@ -40,12 +40,13 @@ namespace pa {
 
 namespace {
 
-// Consumer warps per thread block. Four tensor-core warps (one per
+// Consumer warps per thread block. Four bf16 tensor-core warps (one per
 // scheduler) keep up with HBM, so shared memory goes to the page ring; the
-// CUDA-core consumer is issue-bound and runs eight.
-template <bool TC>
+// uint8 tensor-core and the CUDA-core consumers are latency- or issue-bound
+// and run eight.
+template <int KV, bool TC, int BS>
 constexpr int consumer_warps() {
-  return TC ? 4 : 8;
+  return !TC ? 8 : (KV == PA_KV_BF16 ? 4 : 8);
 }
 constexpr int kMaxSegs = 64;         // segments per window
 constexpr int kMaxWinPages = 1024;   // pages per window (block-table entries staged in smem)
@@ -78,7 +79,7 @@ struct PageGeom {
   static constexpr int kOffVz = kOffVs + kMetaBytes;
 };
 
-template <int KV, int D, int BS, int G, int NS, int W>
+template <int KV, int D, int BS, int G, int NS, int W, bool TC = false>
 struct Smem {
   using PG = PageGeom<KV, D, BS>;
   static constexpr int kStages = W * NS;
@@ -94,7 +95,7 @@ struct Smem {
   static constexpr size_t kStashAccBytes = (size_t)W * G * D * 4;
   static constexpr size_t kOffStashML = kOffStash + kStashAccBytes;
   static constexpr size_t kOffPbuf = kOffStashML + W * G * 2 * 4;
-  static constexpr size_t kPbufBytes = (size_t)W * BS * G * 4;
+  static constexpr size_t kPbufBytes = TC ? 0 : (size_t)W * BS * G * 4;  // CUDA-core consumer only
   static constexpr size_t kOffStages = (kOffPbuf + kPbufBytes + 1023) / 1024 * 1024;
   static constexpr size_t kBytes = kOffStages + (size_t)kStages * PG::kStageBytes + 1024;
 };
@@ -417,9 +418,10 @@ struct FmaConsumer {
 
 // ------------------------------------------------------------------ consumer math (tensor cores)
 //
-// bf16 pools, pages staged by 2-D TMA with 128-byte swizzle: a page is
-// [D/64 halves][BS rows][128 B], and 16-byte chunk c of row r sits at chunk
-// c ^ (r % 8) of its 128-byte row, so ldmatrix reads are conflict-free.
+// bf16 pools, page records staged by 2-D TMA with 128-byte swizzle: a record
+// lands as [D/64 halves][BS K rows, then BS V rows][128 B], and 16-byte chunk
+// c of row r sits at chunk c ^ (r % 8) of its 128-byte row, so ldmatrix reads
+// are conflict-free.
 //
 // Scores of 16 tokens x the 8-wide head group come from mma.m16n8k16
 // (A = K rows, B = Q^T held in registers for the whole unit, fp32
@@ -433,7 +435,8 @@ struct MmaConsumerBf16 {
   static constexpr int KS = D / 16;   // k-steps of the score mma
   static constexpr int MT = D / 16;   // channel tiles of the P.V mma
   static constexpr int TT = BS / 16;  // 16-token tiles per page
-  static constexpr int HALF_BYTES = BS * 128;
+  static constexpr int HALF_BYTES = BS * 128;   // one 64-channel half of K (or V)
+  static constexpr int HALF_STRIDE = 2 * HALF_BYTES;  // a record half: K rows then V rows
   static_assert(G <= 8, "head group");
 
   uint32_t qf[KS][2];
@@ -466,7 +469,7 @@ struct MmaConsumerBf16 {
   __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
     const int lane = threadIdx.x & 31;
     const uint32_t kb = smem_u32(stage);
-    const uint32_t vb = kb + 2 * (D / 64) * HALF_BYTES / 2;  // V follows K
+    const uint32_t vb = kb + HALF_BYTES;  // V rows follow K rows within each half
     // ---- scores S[token][head] for every 16-token tile
     float s[TT][4];
 #pragma unroll
@@ -477,7 +480,7 @@ struct MmaConsumerBf16 {
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int chunk = (ks & 3) * 2 + (lane >> 4);  // 16-byte chunk within the 128-byte half-row
-        const uint32_t addr = kb + (ks >> 2) * HALF_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4);
+        const uint32_t addr = kb + (ks >> 2) * HALF_STRIDE + row * 128 + ((chunk ^ (row & 7)) << 4);
         uint32_t a[4];
         ldmatrix_x4(a, addr);
         mma_bf16_16816(s[tt], a, qf[ks][0], qf[ks][1]);
@@ -533,13 +536,13 @@ struct MmaConsumerBf16 {
     // ---- rows past the sequence end may hold anything: zero them so 0 * x
     // cannot turn into NaN inside the P.V mma
     if (valid < BS) {
-      uint8_t* vrow = stage + (D / 64) * HALF_BYTES;
+      uint8_t* vrow = stage + HALF_BYTES;
       const int n16 = (BS - valid) * (D / 64) * 8;
       for (int i = lane; i < n16; i += 32) {
         const int half = i / ((BS - valid) * 8);
         const int rem = i % ((BS - valid) * 8);
         const int r = valid + rem / 8, c = rem % 8;
-        *reinterpret_cast<uint4*>(vrow + half * HALF_BYTES + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vrow + half * HALF_STRIDE + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
@@ -552,7 +555,7 @@ struct MmaConsumerBf16 {
       for (int mt = 0; mt < MT; ++mt) {
         const int chunk = mt * 2 + (j & 1);  // 16-byte chunk across the 256-byte row
         const int half = chunk >> 3, c = chunk & 7;
-        const uint32_t addr = vb + half * HALF_BYTES + row * 128 + ((c ^ (row & 7)) << 4);
+        const uint32_t addr = vb + half * HALF_STRIDE + row * 128 + ((c ^ (row & 7)) << 4);
         uint32_t a[4];
         ldmatrix_x4_trans(a, addr);
         mma_bf16_16816(o[mt], a, ph[tt][0], ph[tt][1]);
@@ -595,16 +598,294 @@ struct MmaConsumerBf16 {
   }
 };
 
+
+// ------------------------------------------------------------------ consumer math (tensor cores, uint8 KV)
+//
+// uint8 pools with head_dim 128: a page record (K codes, V codes, K scale,
+// K zp, V scale, V zp) is staged by one 2-D TMA box with 128-byte swizzle
+// (16-byte chunk c of 128-byte row r at chunk c ^ (r % 8)). With w_c = q_c * scale_c (per page and
+// head) the score is s_t = sum_c w_c code_tc - sum_c w_c zp_c: the first sum
+// is an f16 mma over exact integer codes (A = K codes, 16 tokens x 16
+// channels per step; B = w, scaled by a power of two so its largest entry
+// sits near 2^13, split into an f16 high part and an f16 remainder), the
+// second an fp32 bias. Channel k-slots are permuted so that lane (g, q)
+// reads channels 16k + 4q .. 16k + 4q + 3 of a row with one 32-bit load.
+// P.V: raw[c][h] = sum_t code_tc p_th by an f16 mma (A = V codes^T gathered
+// from four token rows, B = P^T via movmatrix, P split high + remainder),
+// then o = alpha o + scale_c (raw - zp_c sum_t p_th) per page.
+// Lane (g, q) holds heads 2q, 2q+1 of the online softmax and channels
+// 32p + 4g .. 32p + 4g + 3 (p = 0..3) of the output.
+template <int BS, int G>
+struct MmaConsumerU8 {
+  static constexpr int D = 128;
+  static constexpr int KS = 8;        // 16-channel k-steps
+  static constexpr int TT = BS / 16;  // 16-token tiles per page
+  static constexpr int ROW = 128;     // bytes per token row
+  static constexpr int PAGE = BS * ROW;
+  static_assert(G <= 8, "head group");
+  using PG = PageGeom<PA_KV_UINT8, 128, BS>;
+
+  uint32_t qp[16];  // q[head g] as bf16 pairs: channels 16k + 4q + {0,1} at 2k, {2,3} at 2k+1
+  float o[8][4];    // O^T tile mt = 2p + s: rows -> channels 32p + 4g + 2s + {0, 1}
+  float m0, m1, l0, l1;
+  float scale_log2;
+
+  __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
+    const int lane = threadIdx.x & 31;
+    const int hg = lane >> 2, q4 = (lane & 3) * 4;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      uint2 w = make_uint2(0, 0);
+      if (hg < g) w = *reinterpret_cast<const uint2*>(q_smem + hg * D + 16 * k + q4);
+      qp[2 * k] = w.x;
+      qp[2 * k + 1] = w.y;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.0f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.0f;
+    scale_log2 = sl2;
+  }
+
+  // 16 bytes at byte offset `off` of the swizzled record (off 16-aligned)
+  __device__ __forceinline__ static uint32_t sw(uint32_t base, uint32_t off) {
+    const uint32_t r = off >> 7;
+    return base + (r << 7) + ((((off >> 4) & 7) ^ (r & 7)) << 4);
+  }
+  __device__ __forceinline__ static float4 lds_f4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+  }
+  __device__ __forceinline__ static int4 lds_i4(uint32_t a) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+  }
+
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, q = lane & 3;
+    const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
+    const uint32_t kb = sb + PG::kOffK;
+    const uint32_t vb = sb + PG::kOffV;
+
+    // ---- w = q * scale of head gq and its largest magnitude
+    float w[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const float4 sc = lds_f4(sw(sb, PG::kOffKs + 64 * k + 16 * q));
+      w[4 * k + 0] = bf16_lo(qp[2 * k]) * sc.x;
+      w[4 * k + 1] = bf16_hi(qp[2 * k]) * sc.y;
+      w[4 * k + 2] = bf16_lo(qp[2 * k + 1]) * sc.z;
+      w[4 * k + 3] = bf16_hi(qp[2 * k + 1]) * sc.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(w[4 * k + j]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    ex = ex < 1 ? 1 : ex;
+    int sh = 140 - ex;  // 2^sh * amax lands in [2^13, 2^14)
+    sh = sh < -120 ? -120 : (sh > 120 ? 120 : sh);
+    const float f = __uint_as_float((uint32_t)(127 + sh) << 23);
+    const float finv = __uint_as_float((uint32_t)(127 - sh) << 23);
+
+    // ---- k-steps outermost: B = w * 2^sh split high + remainder (separate
+    // accumulators keep the mma chains short), the zero-point bias, and the
+    // score mma of every 16-token tile
+    float sh_[TT][4], sl_[TT][4];
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sh_[tt][i] = sl_[tt][i] = 0.0f;
+    float bias = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const int4 z = lds_i4(sw(sb, PG::kOffKz + 64 * k + 16 * q));
+      const float w0 = w[4 * k] * f, w1 = w[4 * k + 1] * f, w2 = w[4 * k + 2] * f, w3 = w[4 * k + 3] * f;
+      bias = fmaf(w0, (float)z.x, bias);
+      bias = fmaf(w1, (float)z.y, bias);
+      bias = fmaf(w2, (float)z.z, bias);
+      bias = fmaf(w3, (float)z.w, bias);
+      const uint32_t bh0 = pack_f16(w0, w1), bh1 = pack_f16(w2, w3);
+      const float2 h01 = unpack_f16(bh0), h23 = unpack_f16(bh1);
+      const uint32_t bl0 = pack_f16(w0 - h01.x, w1 - h01.y), bl1 = pack_f16(w2 - h23.x, w3 - h23.y);
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        const int r0 = tt * 16 + gq, r1 = r0 + 8;
+        uint32_t c0, c1;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(kb + r0 * ROW + ((k ^ (r0 & 7)) << 4) + 4 * q) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(kb + r1 * ROW + ((k ^ (r1 & 7)) << 4) + 4 * q) : "memory");
+        uint32_t a[4];
+        a[0] = bytes_to_f16x2(c0, 0x4140);
+        a[1] = bytes_to_f16x2(c1, 0x4140);
+        a[2] = bytes_to_f16x2(c0, 0x4342);
+        a[3] = bytes_to_f16x2(c1, 0x4342);
+        mma_f16_16816(sh_[tt], a, bh0, bh1);
+        mma_f16_16816(sl_[tt], a, bl0, bl1);
+      }
+    }
+    bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+    bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+    // heads 2q, 2q+1 of the score fragments: bias and scale from their lanes
+    const float bias0 = __shfl_sync(0xffffffffu, bias, 8 * q);
+    const float bias1 = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
+    const float mul0 = __shfl_sync(0xffffffffu, finv, 8 * q) * scale_log2;
+    const float mul1 = __shfl_sync(0xffffffffu, finv, 8 * q + 4) * scale_log2;
+    float s[TT][4];
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[tt][i] = sh_[tt][i] + sl_[tt][i];
+    // ---- online softmax for heads 2q, 2q+1
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const bool v0 = tt * 16 + gq < valid, v1 = tt * 16 + gq + 8 < valid;
+      s[tt][0] = v0 ? (s[tt][0] - bias0) * mul0 : -INFINITY;
+      s[tt][1] = v0 ? (s[tt][1] - bias1) * mul1 : -INFINITY;
+      s[tt][2] = v1 ? (s[tt][2] - bias0) * mul0 : -INFINITY;
+      s[tt][3] = v1 ? (s[tt][3] - bias1) * mul1 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    uint32_t ph[TT][2], pl[TT][2];
+    float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
+      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      ps0 += p0 + p2;
+      ps1 += p1 + p3;
+      const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
+      const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
+      ph[tt][0] = movmatrix_trans(h01);
+      ph[tt][1] = movmatrix_trans(h23);
+      pl[tt][0] = movmatrix_trans(pack_f16(p0 - f01.x, p1 - f01.y));
+      pl[tt][1] = movmatrix_trans(pack_f16(p2 - f23.x, p3 - f23.y));
+    }
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+    // page sums of p per head (for the zero-point term of the fold)
+    float sum0 = ps0, sum1 = ps1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      sum0 += __shfl_xor_sync(0xffffffffu, sum0, off);
+      sum1 += __shfl_xor_sync(0xffffffffu, sum1, off);
+    }
+    // ---- raw[c][h] = sum_t code_tc p_th; codes past the sequence end are
+    // finite integers met by p = 0, so they add nothing
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      float raw0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, raw1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const int chunk = 2 * pr + (gq >> 2), cofs = 4 * (gq & 3);
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        const int t0 = tt * 16 + 2 * q, t1 = t0 + 1, t2 = t0 + 8, t3 = t0 + 9;
+        uint32_t W0, W1, W2, W3;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W0) : "r"(vb + t0 * ROW + ((chunk ^ (t0 & 7)) << 4) + cofs) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W1) : "r"(vb + t1 * ROW + ((chunk ^ (t1 & 7)) << 4) + cofs) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W2) : "r"(vb + t2 * ROW + ((chunk ^ (t2 & 7)) << 4) + cofs) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W3) : "r"(vb + t3 * ROW + ((chunk ^ (t3 & 7)) << 4) + cofs) : "memory");
+        const uint32_t u01 = prmt(W0, W1, 0x5140), u23 = prmt(W0, W1, 0x7362);
+        const uint32_t v01 = prmt(W2, W3, 0x5140), v23 = prmt(W2, W3, 0x7362);
+        uint32_t A0[4], A1[4];
+        A0[0] = bytes_to_f16x2(u01, 0x4140);  // channel +0, tokens t0 t1
+        A0[1] = bytes_to_f16x2(u01, 0x4342);  // channel +1
+        A0[2] = bytes_to_f16x2(v01, 0x4140);  // channel +0, tokens t2 t3
+        A0[3] = bytes_to_f16x2(v01, 0x4342);
+        A1[0] = bytes_to_f16x2(u23, 0x4140);  // channel +2
+        A1[1] = bytes_to_f16x2(u23, 0x4342);  // channel +3
+        A1[2] = bytes_to_f16x2(v23, 0x4140);
+        A1[3] = bytes_to_f16x2(v23, 0x4342);
+        mma_f16_16816(raw0, A0, ph[tt][0], ph[tt][1]);
+        mma_f16_16816(raw0, A0, pl[tt][0], pl[tt][1]);
+        mma_f16_16816(raw1, A1, ph[tt][0], ph[tt][1]);
+        mma_f16_16816(raw1, A1, pl[tt][0], pl[tt][1]);
+      }
+      // fold: o = alpha o + scale (raw - zp * sum_p)
+      const int c0 = 32 * pr + 4 * gq;
+      const float4 sc = lds_f4(sw(sb, PG::kOffVs + 4 * c0));
+      const int4 z = lds_i4(sw(sb, PG::kOffVz + 4 * c0));
+      float* oa = o[2 * pr];
+      float* ob = o[2 * pr + 1];
+      oa[0] = fmaf(a0, oa[0], sc.x * fmaf(-(float)z.x, sum0, raw0[0]));
+      oa[1] = fmaf(a1, oa[1], sc.x * fmaf(-(float)z.x, sum1, raw0[1]));
+      oa[2] = fmaf(a0, oa[2], sc.y * fmaf(-(float)z.y, sum0, raw0[2]));
+      oa[3] = fmaf(a1, oa[3], sc.y * fmaf(-(float)z.y, sum1, raw0[3]));
+      ob[0] = fmaf(a0, ob[0], sc.z * fmaf(-(float)z.z, sum0, raw1[0]));
+      ob[1] = fmaf(a1, ob[1], sc.z * fmaf(-(float)z.z, sum1, raw1[1]));
+      ob[2] = fmaf(a0, ob[2], sc.w * fmaf(-(float)z.w, sum0, raw1[2]));
+      ob[3] = fmaf(a1, ob[3], sc.w * fmaf(-(float)z.w, sum1, raw1[3]));
+    }
+  }
+
+  __device__ __forceinline__ void deposit(float* st_acc, float* st_ml) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, q = lane & 3;
+    float s0 = l0, s1 = l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    const int h0 = 2 * q;
+    if (lane < 4) {
+      if (h0 < G) {
+        st_ml[h0 * 2] = m0;
+        st_ml[h0 * 2 + 1] = s0;
+      }
+      if (h0 + 1 < G) {
+        st_ml[(h0 + 1) * 2] = m1;
+        st_ml[(h0 + 1) * 2 + 1] = s1;
+      }
+    }
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+#pragma unroll
+      for (int sd = 0; sd < 2; ++sd) {
+        const int c = 32 * pr + 4 * gq + 2 * sd;
+        const float* ot = o[2 * pr + sd];
+        if (h0 < G) {
+          st_acc[h0 * D + c] = ot[0];
+          st_acc[h0 * D + c + 1] = ot[2];
+        }
+        if (h0 + 1 < G) {
+          st_acc[(h0 + 1) * D + c] = ot[1];
+          st_acc[(h0 + 1) * D + c + 1] = ot[3];
+        }
+      }
+    }
+  }
+};
+
 // ------------------------------------------------------------------ the decode kernel
 template <int KV, int D, int BS, int G, int NS, bool TC>
-__global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
+__global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
     paged_gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int kConsumerWarps = consumer_warps<TC>();
+  constexpr int kConsumerWarps = consumer_warps<KV, TC, BS>();
   constexpr int kThreads = (kConsumerWarps + 1) * 32;
-  using SM = Smem<KV, D, BS, G, NS, kConsumerWarps>;
+  using SM = Smem<KV, D, BS, G, NS, kConsumerWarps, TC>;
   using PG = PageGeom<KV, D, BS>;
-  using Cons = typename std::conditional<TC, MmaConsumerBf16<D, BS, G>, FmaConsumer<KV, D, BS, G>>::type;
-  static_assert(!TC || KV == PA_KV_BF16, "tensor-core consumer reads bf16 pages");
+  using Cons = typename std::conditional<
+      TC,
+      typename std::conditional<KV == PA_KV_BF16, MmaConsumerBf16<D, BS, G>, MmaConsumerU8<BS, G>>::type,
+      FmaConsumer<KV, D, BS, G>>::type;
+  static_assert(!TC || KV == PA_KV_BF16 || (KV == PA_KV_UINT8 && D == 128),
+                "tensor-core consumers: bf16 pages, or uint8 pages of head_dim 128");
   constexpr int NST = SM::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled TMA destinations
@@ -880,24 +1161,18 @@ __global__ void __launch_bounds__((consumer_warps<TC>() + 1) * 32, 1)
             const long long page = (long long)phys * Hkv + sg.h;
             issued_n[stage] = n;
             mbar_arrive_expect_tx(&full[stage], PG::kStageBytes);
-            if (TC) {
-              // two 64-channel boxes per tensor (one for head_dim 64), swizzled
+            if (TC && KV == PA_KV_UINT8) {
+              // the whole record as one box of 128-byte rows, swizzled
+              tma_load_2d(dst, &p.maps.rec, 0, (int)(page * p.maps.rows_per_page), &full[stage], pol);
+            } else if (TC) {
+              // one box of 64 channels x (K and V rows) per half, swizzled
 #pragma unroll
-              for (int hf = 0; hf < D / 64; ++hf) {
-                tma_load_2d(dst + PG::kOffK + hf * BS * 128, &p.maps.k, hf * 64, (int)(page * BS),
+              for (int hf = 0; hf < D / 64; ++hf)
+                tma_load_2d(dst + hf * 2 * BS * 128, &p.maps.rec, hf * 64, (int)(page * 2 * BS),
                             &full[stage], pol);
-                tma_load_2d(dst + PG::kOffV + hf * BS * 128, &p.maps.v, hf * 64, (int)(page * BS),
-                            &full[stage], pol);
-              }
             } else {
-              bulk_g2s(dst + PG::kOffK, p.pool.k + page * PG::kPageBytes, PG::kPageBytes, &full[stage], pol);
-              bulk_g2s(dst + PG::kOffV, p.pool.v + page * PG::kPageBytes, PG::kPageBytes, &full[stage], pol);
-            }
-            if (KV != PA_KV_BF16) {
-              bulk_g2s(dst + PG::kOffKs, p.pool.k_scale + page * D, PG::kMetaBytes, &full[stage], pol);
-              bulk_g2s(dst + PG::kOffKz, p.pool.k_zp + page * D, PG::kMetaBytes, &full[stage], pol);
-              bulk_g2s(dst + PG::kOffVs, p.pool.v_scale + page * D, PG::kMetaBytes, &full[stage], pol);
-              bulk_g2s(dst + PG::kOffVz, p.pool.v_zp + page * D, PG::kMetaBytes, &full[stage], pol);
+              // the whole record, unswizzled
+              bulk_g2s(dst, page_of(p.pool.k, page, p.pool.stride), PG::kStageBytes, &full[stage], pol);
             }
           }
         }
@@ -1057,7 +1332,7 @@ __global__ void __launch_bounds__(256)
 
 template <int KV, int D, int BS, int G, int NS, bool TC>
 cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t stream) {
-  using SM = Smem<KV, D, BS, G, NS, consumer_warps<TC>()>;
+  using SM = Smem<KV, D, BS, G, NS, consumer_warps<KV, TC, BS>(), TC>;
   auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC>;
   static bool attr_set = false;  // per instantiation; set before first launch
   if (!attr_set) {
@@ -1070,7 +1345,7 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.num_ctas);
-  cfg.blockDim = dim3((consumer_warps<TC>() + 1) * 32);
+  cfg.blockDim = dim3((consumer_warps<KV, TC, BS>() + 1) * 32);
   cfg.dynamicSmemBytes = SM::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -1092,33 +1367,33 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
 // allows next to the fixed parts (1..8 per warp, largest that fits with 1 KB
 // of static shared memory to spare). Bytes in flight per SM are what sustains
 // HBM bandwidth (Little's law), so the ring gets the rest.
-template <int KV, int D, int BS, int W, int N>
+template <int KV, int D, int BS, int G, int W, bool TC, int N>
 constexpr int largest_ring() {
   if constexpr (N <= 1) {
     return 1;
-  } else if constexpr (Smem<KV, D, BS, 8, N, W>::kBytes + 1024 <= 227 * 1024) {
+  } else if constexpr (Smem<KV, D, BS, G, N, W, TC>::kBytes + 1024 <= 227 * 1024) {
     return N;
   } else {
-    return largest_ring<KV, D, BS, W, N - 1>();
+    return largest_ring<KV, D, BS, G, W, TC, N - 1>();
   }
 }
 
-template <int KV, int D, int BS, int W>
+template <int KV, int D, int BS, int G, int W, bool TC>
 constexpr int stages_per_warp() {
-  return largest_ring<KV, D, BS, W, 8>();
+  return largest_ring<KV, D, BS, G, W, TC, 8>();
 }
 
 template <int KV, int D, int BS, bool TC>
 cudaError_t dispatch_g(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
-  constexpr int NS = stages_per_warp<KV, D, BS, consumer_warps<TC>()>();
-  if (L.group <= 2) return launch_t<KV, D, BS, 2, NS, TC>(prm, L, s);
-  if (L.group <= 4) return launch_t<KV, D, BS, 4, NS, TC>(prm, L, s);
-  return launch_t<KV, D, BS, 8, NS, TC>(prm, L, s);
+  constexpr int W = consumer_warps<KV, TC, BS>();
+  if (L.group <= 2) return launch_t<KV, D, BS, 2, stages_per_warp<KV, D, BS, 2, W, TC>(), TC>(prm, L, s);
+  if (L.group <= 4) return launch_t<KV, D, BS, 4, stages_per_warp<KV, D, BS, 4, W, TC>(), TC>(prm, L, s);
+  return launch_t<KV, D, BS, 8, stages_per_warp<KV, D, BS, 8, W, TC>(), TC>(prm, L, s);
 }
 
 template <int KV, int D, int BS>
 cudaError_t dispatch_path(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
-  if constexpr (KV == PA_KV_BF16) {
+  if constexpr (KV == PA_KV_BF16 || (KV == PA_KV_UINT8 && D == 128)) {
     if (L.tensor_cores) return dispatch_g<KV, D, BS, true>(prm, L, s);
   }
   return dispatch_g<KV, D, BS, false>(prm, L, s);
@@ -1138,12 +1413,14 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 template <int KV, int D, int BS, bool TC>
 size_t smem_bytes_g(int group) {
-  constexpr int W = consumer_warps<TC>();
-  constexpr int NS = stages_per_warp<KV, D, BS, W>();
-  static_assert(Smem<KV, D, BS, 8, NS, W>::kBytes <= 227 * 1024, "shared memory budget");
-  if (group <= 2) return Smem<KV, D, BS, 2, NS, W>::kBytes;
-  if (group <= 4) return Smem<KV, D, BS, 4, NS, W>::kBytes;
-  return Smem<KV, D, BS, 8, NS, W>::kBytes;
+  constexpr int W = consumer_warps<KV, TC, BS>();
+  constexpr int N2 = stages_per_warp<KV, D, BS, 2, W, TC>();
+  constexpr int N4 = stages_per_warp<KV, D, BS, 4, W, TC>();
+  constexpr int N8 = stages_per_warp<KV, D, BS, 8, W, TC>();
+  static_assert(Smem<KV, D, BS, 8, N8, W, TC>::kBytes <= 227 * 1024, "shared memory budget");
+  if (group <= 2) return Smem<KV, D, BS, 2, N2, W, TC>::kBytes;
+  if (group <= 4) return Smem<KV, D, BS, 4, N4, W, TC>::kBytes;
+  return Smem<KV, D, BS, 8, N8, W, TC>::kBytes;
 }
 
 template <int KV, bool TC>
@@ -1156,7 +1433,7 @@ size_t smem_bytes_kv(int D, int BS, int group) {
 
 }  // namespace
 
-bool make_pool_maps(const PoolDev& pool, PoolMaps& maps) {
+bool make_pool_maps(int kv_dtype, const PoolDev& pool, PoolMaps& maps) {
   maps.valid = 0;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -1168,20 +1445,22 @@ bool make_pool_maps(const PoolDev& pool, PoolMaps& maps) {
                                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill)>(fn);
-  const unsigned long long rows =
-      (unsigned long long)pool.num_blocks * pool.num_kv_heads * pool.block_size;
-  if (rows >= (1ull << 31)) return false;  // row coordinates are int32
-  const cuuint64_t gdim[2] = {(cuuint64_t)pool.head_dim, (cuuint64_t)rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)pool.head_dim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)pool.block_size};
+  const bool u8 = kv_dtype == PA_KV_UINT8;
+  if (u8 && pool.head_dim != 128) return false;
+  const unsigned long long pages = (unsigned long long)pool.num_blocks * pool.num_kv_heads;
+  const int rpp = u8 ? (int)(pool.stride / 128) : 2 * pool.block_size;  // rows per record
+  const unsigned long long rows = pages * (unsigned long long)rpp;
+  if (rows >= (1ull << 31) || rpp > 256) return false;  // row coordinates are int32; box <= 256 rows
+  const cuuint64_t gdim[2] = {(cuuint64_t)(u8 ? 128 : pool.head_dim), (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)(u8 ? 128 : pool.head_dim * 2)};
+  const cuuint32_t box[2] = {u8 ? 128u : 64u, (cuuint32_t)rpp};
   const cuuint32_t estr[2] = {1, 1};
-  for (int t = 0; t < 2; ++t) {
-    CUresult r = encode(t == 0 ? &maps.k : &maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                        t == 0 ? (void*)pool.k : (void*)pool.v, gdim, gstride, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return false;
-  }
+  CUresult r = encode(&maps.rec, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                      (void*)pool.k, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  maps.rows_per_page = rpp;
   maps.valid = 1;
   return true;
 }
@@ -1197,7 +1476,9 @@ int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bo
   size_t smem = kv_dtype == PA_KV_BF16
                     ? (tensor_cores ? smem_bytes_kv<PA_KV_BF16, true>(head_dim, block_size, group)
                                     : smem_bytes_kv<PA_KV_BF16, false>(head_dim, block_size, group))
-                : kv_dtype == PA_KV_UINT8 ? smem_bytes_kv<PA_KV_UINT8, false>(head_dim, block_size, group)
+                : kv_dtype == PA_KV_UINT8
+                    ? (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_UINT8, true>(head_dim, block_size, group)
+                                                       : smem_bytes_kv<PA_KV_UINT8, false>(head_dim, block_size, group))
                                           : smem_bytes_kv<PA_KV_UINT4, false>(head_dim, block_size, group);
   const size_t per_sm = 227 * 1024;
   int n = (int)(per_sm / (smem + 1024));

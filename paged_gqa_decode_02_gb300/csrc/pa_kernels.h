@@ -39,9 +39,10 @@ size_t decode_workspace_bytes(int num_ctas, int batch, int num_kv_heads, int gro
 // Thread blocks of the decode kernel that fit on one SM for this shape.
 int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bool tensor_cores);
 
-// Encode the TMA descriptors of a bf16 pool (false if the driver call fails
-// or the pool is too large for 32-bit row coordinates).
-bool make_pool_maps(const PoolDev& pool, PoolMaps& maps);
+// Encode the TMA descriptors of a bf16 pool, or of a uint8 pool with head_dim
+// 128 (false if the driver call fails, the shape is not served or the pool is
+// too large for 32-bit row coordinates).
+bool make_pool_maps(int kv_dtype, const PoolDev& pool, PoolMaps& maps);
 
 // Carve the workspace and launch decode + combine.
 cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& maps, const void* q,

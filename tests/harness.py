@@ -29,15 +29,15 @@ def dev(a, dtype=None):
 
 def host_pool_arrays(gpool):
     """Copy a GPU pool to numpy, in the oracle's naming."""
-    v = gpool.view()
+    v = {k: np.ascontiguousarray(t.contiguous().cpu().numpy()) for k, t in gpool.view().items()}
     out = {}
     if gpool.kv_dtype == "bf16":
-        out["k16"] = v["k"].cpu().numpy().view(np.uint16)
-        out["v16"] = v["v"].cpu().numpy().view(np.uint16)
+        out["k16"] = v["k"].view(np.uint16)
+        out["v16"] = v["v"].view(np.uint16)
     else:
-        out["kc"], out["vc"] = v["k"].cpu().numpy(), v["v"].cpu().numpy()
-        out["ks"], out["vs"] = v["k_scale"].cpu().numpy(), v["v_scale"].cpu().numpy()
-        out["kz"], out["vz"] = v["k_zp"].cpu().numpy(), v["v_zp"].cpu().numpy()
+        out["kc"], out["vc"] = v["k"], v["v"]
+        out["ks"], out["vs"] = v["k_scale"], v["v_scale"]
+        out["kz"], out["vz"] = v["k_zp"], v["v_zp"]
     return out
 
 

@@ -16,8 +16,12 @@ def _built():
     build.build()
 
 
-def _paths(dt):
-    return ["cuda_core", "tensor_core"] if dt == "bf16" else ["cuda_core"]
+def _paths(dt, head_dim=128):
+    """Decode kernels that serve a pool: tensor cores for bf16, and for uint8
+    with head_dim 128; the CUDA-core kernel everywhere."""
+    if dt == "bf16" or (dt == "uint8" and head_dim == 128):
+        return ["cuda_core", "tensor_core"]
+    return ["cuda_core"]
 
 
 @pytest.mark.parametrize("combine", ["fused", "separate"])
@@ -42,7 +46,7 @@ def test_random_small(seed, dt):
     H.assert_pools_equal(g, o)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
-    for path in _paths(dt):
+    for path in _paths(dt, wl.head_dim):
         for splits in (0, 1, 5, 10 ** 4):
             for combine in ("fused", "separate"):
                 got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
@@ -66,7 +70,7 @@ def test_multi_step_tail_requant(dt):
         assert o.append_call(step) == 0
         H.assert_pools_equal(g, o)
         ref, _ = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
-        for path in _paths(dt):
+        for path in _paths(dt, wl.head_dim):
             H.check_attention(H.gpu_decode(g, wl, path=path), ref, f"steps {dt} {path}")
 
 
@@ -133,7 +137,7 @@ def test_full_size_config(name):
     rows = H.sample_rows(wl)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
     assert st == 0
-    for path in _paths(wl.kv_dtype):
+    for path in _paths(wl.kv_dtype, wl.head_dim):
         for splits, combine in ((0, "fused"), (97, "fused"), (0, "separate")):
             got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
             H.check_attention(got[rows], ref, f"{name} splits={splits} {path} {combine}")
@@ -151,7 +155,7 @@ def test_slices_longer_than_a_window(dt):
     H.assert_pools_equal(g, o)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
-    for path in _paths(dt):
+    for path in _paths(dt, wl.head_dim):
         for splits in (1, 2, 3):
             got = H.gpu_decode(g, wl, num_splits=splits, path=path)
             H.check_attention(got, ref, f"long slices {dt} splits={splits} {path}")
