@@ -163,7 +163,8 @@ def run_ours(args):
     wl = W.CONFIGS[args.workload]()
     dev = torch.device("cuda", local)
     pool = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, local)
-    pool.set_decode_path(args.path, fused_combine=(args.combine == "fused"))
+    pool.set_decode_path(args.path, fused_combine=(args.combine == "fused"),
+                         early_plan=not args.no_early_plan)
 
     def d(a):
         a = np.ascontiguousarray(a)
@@ -185,11 +186,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def one_step():
+        # append then decode back to back, as a decode loop runs them (the
+        # decode's planning may overlap the append; see --no-early-plan)
         pool.append_kv(st_k, st_v, st_cu, st_ctx, table, max_new_per_seq=1)
-        e_mid = torch.cuda.Event(enable_timing=True)
-        e_mid.record(stream)
         pool.decode(q, table, seq_lens, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
-        return e_mid
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
@@ -210,19 +210,28 @@ def run_ours(args):
     K = args.steps
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e1 = []
     _barrier(dist)
     torch.cuda.synchronize()
     for i in range(K):
         flush.fill_(1)
         e0[i].record(stream)
-        e1.append(one_step())
+        one_step()
         e2[i].record(stream)
     torch.cuda.synchronize()
     _barrier(dist)
+    # roofline of the decode call alone: a second pass of K calls, each
+    # bracketed by events (L2 flushed before each)
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(1)
+        d0[i].record(stream)
+        pool.decode(q, table, seq_lens, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
+        d1[i].record(stream)
+    torch.cuda.synchronize()
     clk = clocks.stop()
     step_ms = [e0[i].elapsed_time(e2[i]) for i in range(K)]
-    dec_ms = [e1[i].elapsed_time(e2[i]) for i in range(K)]
+    dec_ms = [d0[i].elapsed_time(d1[i]) for i in range(K)]
     st, flags = pool.device_error()
     assert st == 0 and flags == 0, f"device error word {flags:#x} during timing"
     t_step = statistics.mean(step_ms) / 1e3
@@ -281,6 +290,7 @@ def run_ours(args):
                    "step": "append 1 token/seq (kv_quant_append) + paged_gqa_decode (split-KV merge: "
                            + args.combine + ")",
                    "decode_path": args.path,
+                   "early_plan": not args.no_early_plan,
                    "l2": "flushed before every timed step (256 MiB write, outside the event brackets)",
                    "parallelism": f"replicas x{world} (no exchange)"},
         "hbm_gbs": achieved,
@@ -291,7 +301,8 @@ def run_ours(args):
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": nb["algorithmic"],
-                     "timed": "pa_decode call (decode kernel + split-KV combine), CUDA events on the launch stream"},
+                     "timed": "pa_decode call (decode kernel + split-KV combine) alone, CUDA events on the "
+                              "launch stream, a second pass of K calls after the K timed steps"},
         "e2e": {"value": world * B / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": 3 * K,
@@ -386,6 +397,8 @@ def main():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core"])
     ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
+    ap.add_argument("--no-early-plan", action="store_true",
+                    help="decode plans only after the append kernel has finished")
     ap.add_argument("--cpu-seqs", type=int, default=1 << 30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -192,13 +192,19 @@ PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
  * the same operation. Sequences cut by slice boundaries are merged by a
  * separate log-sum-exp combine kernel; OR-ing PA_DECODE_FUSED_COMBINE merges
  * them inside the decode kernel instead (the last slice to finish a sequence
- * merges its partials, found through call-tagged tickets).
+ * merges its partials, found through call-tagged tickets). OR-ing
+ * PA_DECODE_EARLY_PLAN lets the decode kernel read seq_lens and block_table
+ * (and plan its work) while the kernel launched just before it on the stream
+ * is still running; it still waits for that kernel before reading any page or
+ * writing anything. Set it only when that preceding kernel writes neither
+ * seq_lens nor block_table (pa_append_kv writes neither).
  * PA_ERR_UNSUPPORTED if TENSOR_CORE is asked for a pool it does not serve. */
 typedef enum {
   PA_DECODE_AUTO = 0,
   PA_DECODE_CUDA_CORE = 1,
   PA_DECODE_TENSOR_CORE = 2,
-  PA_DECODE_FUSED_COMBINE = 4
+  PA_DECODE_FUSED_COMBINE = 4,
+  PA_DECODE_EARLY_PLAN = 8
 } pa_decode_path;
 PA_API pa_status pa_pool_set_decode_path(pa_pool* pool, int32_t path);
 

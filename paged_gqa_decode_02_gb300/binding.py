@@ -138,6 +138,7 @@ def pa_decode_workspace_bytes(handle, batch, num_q_heads, num_splits=0):
 
 PA_DECODE_AUTO, PA_DECODE_CUDA_CORE, PA_DECODE_TENSOR_CORE = 0, 1, 2
 PA_DECODE_FUSED_COMBINE = 4
+PA_DECODE_EARLY_PLAN = 8
 DECODE_PATHS = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
 
 
@@ -220,12 +221,15 @@ class PagedKVPool:
         pa_append_kv(self.handle, k_new, v_new, cu_new, ctx_lens, block_table, B,
                      int(block_table.shape[1]) if B else 0, max_new_per_seq, stream)
 
-    def set_decode_path(self, path, fused_combine=False):
+    def set_decode_path(self, path, fused_combine=False, early_plan=False):
         """'auto', 'cuda_core' or 'tensor_core'; split sequences are merged by
         the separate combine kernel, or inside the decode kernel with
-        fused_combine (see pa_pool_set_decode_path)."""
+        fused_combine; early_plan overlaps the decode's planning with the
+        preceding kernel (see pa_pool_set_decode_path)."""
         code = DECODE_PATHS[path] if isinstance(path, str) else int(path)
-        pa_pool_set_decode_path(self.handle, code | (PA_DECODE_FUSED_COMBINE if fused_combine else 0))
+        code |= PA_DECODE_FUSED_COMBINE if fused_combine else 0
+        code |= PA_DECODE_EARLY_PLAN if early_plan else 0
+        pa_pool_set_decode_path(self.handle, code)
 
     def workspace_bytes(self, batch, num_q_heads, num_splits=0):
         return pa_decode_workspace_bytes(self.handle, batch, num_q_heads, num_splits)

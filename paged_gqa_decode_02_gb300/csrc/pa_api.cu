@@ -16,6 +16,7 @@ struct pa_pool {
   pa_pool_desc desc;
   int32_t decode_path;
   bool fused_combine;
+  bool early_plan;
   void* slab;
   size_t slab_bytes;
   pa::PoolDev dev;
@@ -170,6 +171,7 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   }
   p->decode_path = PA_DECODE_AUTO;
   p->fused_combine = false;
+  p->early_plan = false;
   p->maps.valid = 0;
   if (d->kv_dtype != PA_KV_UINT4) pa::make_pool_maps(d->kv_dtype, p->dev, p->maps);
   *out = p;
@@ -246,12 +248,14 @@ pa_status pa_pool_set_decode_path(pa_pool* p, int32_t path) {
   g_last_error[0] = 0;
   if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
   const int kernel = path & 3;
-  if (path < 0 || (path & ~(3 | PA_DECODE_FUSED_COMBINE)) || kernel > PA_DECODE_TENSOR_CORE)
+  if (path < 0 || (path & ~(3 | PA_DECODE_FUSED_COMBINE | PA_DECODE_EARLY_PLAN)) ||
+      kernel > PA_DECODE_TENSOR_CORE)
     return fail(PA_ERR_INVALID_ARG, "unknown decode path%s");
   if (kernel == PA_DECODE_TENSOR_CORE && !p->maps.valid)
     return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path serves bf16 pools and uint8 pools of head_dim 128%s");
   p->decode_path = kernel;
   p->fused_combine = (path & PA_DECODE_FUSED_COMBINE) != 0;
+  p->early_plan = (path & PA_DECODE_EARLY_PLAN) != 0;
   return PA_OK;
 }
 
@@ -303,6 +307,7 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   L.scale_log2 = softmax_scale * 1.4426950408889634f;
   L.tensor_cores = uses_tensor_cores(p);
   L.fused_combine = p->fused_combine;
+  L.early_plan = p->early_plan;
   L.epoch = next_epoch();
   cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
                                     workspace, L, static_cast<cudaStream_t>(stream));

@@ -113,6 +113,8 @@ struct DecodeParams {
   unsigned long long* tickets;  // per unit: (epoch << 24) | slices finished
   unsigned long long epoch;     // 40-bit call tag, never 0
   int fused;                    // merge split units in this kernel (else: combine kernel)
+  int early_plan;               // plan (reads of lengths / tables only) before waiting
+                                // on the preceding kernel
   int batch;
   int num_q_heads;
   int group;
@@ -915,10 +917,17 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
   __shared__ int merge_flag;
 
   // Launched with programmatic stream serialization: let the combine kernel
-  // be scheduled early, but touch no global memory before the preceding
-  // kernel in the stream has completed.
+  // be scheduled early; write no global memory and read no page before the
+  // preceding kernel in the stream has completed. With early_plan the caller
+  // vouches that the preceding kernel writes neither the lengths nor the
+  // block table, so the read-only planning below (lengths, slice, segment
+  // list, block-table entries) overlaps it.
   pdl_launch_dependents();
-  pdl_wait();
+  bool waited = false;
+  if (!p.early_plan) {
+    pdl_wait();
+    waited = true;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -967,10 +976,6 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
       const int incl = block_incl_scan(n, warp_tot, tot);
       const long long lo = (long long)(running + incl - n) * Hkv;
       const long long hi = (long long)(running + incl) * Hkv;
-      if (cta == 0 && b < p.batch) {
-        p.pre_pages[b] = running + incl - n;
-        if (b == p.batch - 1) p.pre_pages[p.batch] = running + incl;
-      }
       if (b < p.batch && s_i >= lo && s_i < hi) {
         plan[0] = b;
         plan[1] = lo;
@@ -983,8 +988,31 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
         if (found) break;
       }
     }
-    if (cta == 0 && p.batch == 0 && tid == 0) p.pre_pages[0] = 0;
-    if (cta == 0 && p.fused) {
+  }
+  // CTA 0 publishes the per-sequence page prefix for the combine kernel (and,
+  // with the in-kernel merge, zero rows for empty sequences): global writes,
+  // so after the wait. lens_sm is still intact (no merge has run yet).
+  bool published = false;
+  auto wait_and_publish = [&]() {
+    if (published) return;
+    published = true;
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+    if (cta != 0) return;
+    int running = 0;
+    for (int base = 0; base < p.batch; base += kThreads) {
+      const int b = base + tid;
+      const int n = b < p.batch ? ((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS : 0;
+      int tot;
+      const int incl = block_incl_scan(n, warp_tot, tot);
+      if (b < p.batch) p.pre_pages[b] = running + incl - n;
+      if (b == p.batch - 1) p.pre_pages[p.batch] = running + incl;
+      running += tot;
+    }
+    if (p.batch == 0 && tid == 0) p.pre_pages[0] = 0;
+    if (p.fused) {
       // rows of empty sequences: no slice holds a page of them
       const int row_elems = p.num_q_heads * D;
       for (int b = 0; b < p.batch; ++b) {
@@ -993,9 +1021,14 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
           for (int e = tid; e < row_elems; e += kThreads) p.out[(long long)b * row_elems + e] = 0.0f;
       }
     }
-  }
+    __syncthreads();
+  };
+  if (!p.early_plan) wait_and_publish();
   __syncthreads();
-  if (s_i >= e_i) return;  // no pages for this thread block
+  if (s_i >= e_i) {  // no pages for this thread block
+    wait_and_publish();
+    return;
+  }
 
   long long cur_b = plan[0], cur_base = plan[1];  // sequence holding `pos` and its first page
   long long pos = s_i;
@@ -1092,18 +1125,20 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
     const int kw0 = (int)(pos - s_i), kw1 = (int)(wend - s_i);
 
     if (warp == 0) {
-      // ---------------------------------------------------------- producer
       // (1) the window's block-table entries -> shared memory, all lanes
-      {
-        int sx = 0;
-        for (int i = lane; i < kw1 - kw0; i += 32) {
-          const int k = kw0 + i;
-          while (sx + 1 < nseg && k >= segs[sx + 1].k0) ++sx;
-          const Seg& sg = segs[sx];
-          phys_s[i] = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
-        }
-        __syncwarp();
+      int sx = 0;
+      for (int i = lane; i < kw1 - kw0; i += 32) {
+        const int k = kw0 + i;
+        while (sx + 1 < nseg && k >= segs[sx + 1].k0) ++sx;
+        const Seg& sg = segs[sx];
+        phys_s[i] = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
       }
+      __syncwarp();
+    }
+    wait_and_publish();  // first window only: pages and outputs follow
+
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
       // (2) issue in sub-batches, lane j taking page k + j. A sub-batch holds
       // at most one page per stage (<= NST pages): the previous fill of each
       // lane's stage was issued by an earlier sub-batch, after the release of
@@ -1510,6 +1545,7 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& map
   prm.tickets = tickets;
   prm.epoch = L.epoch;
   prm.fused = L.fused_combine ? 1 : 0;
+  prm.early_plan = L.early_plan ? 1 : 0;
   prm.batch = L.batch;
   prm.num_q_heads = L.num_q_heads;
   prm.group = L.group;

@@ -21,6 +21,7 @@ struct DecodeLaunch {
   float scale_log2;     // softmax_scale * log2(e)
   bool tensor_cores;    // bf16 pools: mma consumer fed by swizzled 2-D TMA
   bool fused_combine;   // merge split units inside the decode kernel
+  bool early_plan;      // plan before waiting on the preceding kernel
   unsigned long long epoch;  // per-call tag of the merge tickets (40 bits, never 0)
   // workspace carve-up
   int32_t* pre_pages;   // [batch + 1] prefix sums of per-sequence block counts

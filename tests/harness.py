@@ -86,9 +86,10 @@ def assert_pools_equal(gpool, opool):
             raise AssertionError(f"pool array {name} differs at {len(diff)} places, first {diff[:5].tolist()}")
 
 
-def gpu_decode(gpool, wl, num_splits=0, out_fill=float("nan"), path="auto", combine="separate"):
+def gpu_decode(gpool, wl, num_splits=0, out_fill=float("nan"), path="auto", combine="separate",
+               early_plan=False):
     torch = torch_mod()
-    gpool.set_decode_path(path, fused_combine=(combine == "fused"))
+    gpool.set_decode_path(path, fused_combine=(combine == "fused"), early_plan=early_plan)
     out = torch.full((wl.batch, wl.num_q_heads, wl.head_dim), out_fill, dtype=torch.float32,
                      device="cuda")
     gpool.decode(dev(wl.q_bits), dev(wl.block_table), dev(wl.seq_lens), wl.softmax_scale, out=out,

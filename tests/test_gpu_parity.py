@@ -49,7 +49,8 @@ def test_random_small(seed, dt):
     for path in _paths(dt, wl.head_dim):
         for splits in (0, 1, 5, 10 ** 4):
             for combine in ("fused", "separate"):
-                got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
+                got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine,
+                                   early_plan=(splits % 2 == 1))
                 H.check_attention(got, ref, f"{wl.name} {dt} splits={splits} {path} {combine}")
     assert g.device_error() == (0, 0)
 
@@ -138,9 +139,10 @@ def test_full_size_config(name):
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
     assert st == 0
     for path in _paths(wl.kv_dtype, wl.head_dim):
-        for splits, combine in ((0, "fused"), (97, "fused"), (0, "separate")):
-            got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
-            H.check_attention(got[rows], ref, f"{name} splits={splits} {path} {combine}")
+        for splits, combine, early in ((0, "fused", False), (97, "fused", True), (0, "separate", True),
+                                       (0, "separate", False)):
+            got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine, early_plan=early)
+            H.check_attention(got[rows], ref, f"{name} splits={splits} {path} {combine} early={early}")
             assert np.isfinite(got).all()
     assert g.device_error() == (0, 0)
 
