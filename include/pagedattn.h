@@ -185,7 +185,7 @@ PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int3
 PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
 
 /* Decode kernel selection for a pool. AUTO uses the tensor-core kernel where
- * it is built (bf16 pools, and uint8 pools of head_dim 128: scores and P.V as
+ * it is built (bf16 pools, and uint8 / uint4 pools of head_dim 128: scores and P.V as
  * mma.m16n8k16 over the GQA group, pages staged by swizzled 2-D TMA) and the
  * CUDA-core kernel otherwise;
  * CUDA_CORE forces the fp32 FMA kernel (kept for comparison). Both compute

@@ -173,7 +173,7 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   p->fused_combine = false;
   p->early_plan = false;
   p->maps.valid = 0;
-  if (d->kv_dtype != PA_KV_UINT4) pa::make_pool_maps(d->kv_dtype, p->dev, p->maps);
+  pa::make_pool_maps(d->kv_dtype, p->dev, p->maps);
   *out = p;
   return PA_OK;
 }
@@ -252,7 +252,7 @@ pa_status pa_pool_set_decode_path(pa_pool* p, int32_t path) {
       kernel > PA_DECODE_TENSOR_CORE)
     return fail(PA_ERR_INVALID_ARG, "unknown decode path%s");
   if (kernel == PA_DECODE_TENSOR_CORE && !p->maps.valid)
-    return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path serves bf16 pools and uint8 pools of head_dim 128%s");
+    return fail(PA_ERR_UNSUPPORTED, "the tensor-core decode path serves bf16 pools and quantised pools of head_dim 128%s");
   p->decode_path = kernel;
   p->fused_combine = (path & PA_DECODE_FUSED_COMBINE) != 0;
   p->early_plan = (path & PA_DECODE_EARLY_PLAN) != 0;

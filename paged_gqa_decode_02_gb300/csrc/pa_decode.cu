@@ -874,6 +874,293 @@ struct MmaConsumerU8 {
   }
 };
 
+
+// ------------------------------------------------------------------ consumer math (tensor cores, uint4 KV)
+//
+// Packed uint4 pools with head_dim 128: like the uint8 consumer, on a page
+// record of 64-byte token rows (two per 128-byte swizzled row). A 32-bit load
+// of a token row carries 8 channels as nibbles (channel 2i low, 2i+1 high);
+// masking gives the even channels, a shift the odd ones, each as bytes that
+// become exact f16 integers. Scores: lane (g, q) loads bytes 16k + 4q of a
+// row = channels 32k + 8q .. +7 and feeds two k-steps with them (even
+// channels in the first B/A slots, odd in the second); B = w for the same
+// channels. P.V: lane (g, q) owns channels 64o + 8g + 2s + {0, 1} of the
+// O^T tiles 4o + s and gathers them from four token rows.
+template <int BS, int G>
+struct MmaConsumerU4 {
+  static constexpr int D = 128;
+  static constexpr int TT = BS / 16;
+  static constexpr int ROWB = 64;  // bytes per token row
+  static_assert(G <= 8, "head group");
+  using PG = PageGeom<PA_KV_UINT4, 128, BS>;
+
+  uint32_t qp[16];  // q[head g] bf16 pairs, channels 32k + 8q + {0,1},{2,3},{4,5},{6,7} at 4k..4k+3
+  float o[8][4];    // O^T tile mt = 4o + s: rows -> channels 64o + 8g + 2s + {0, 1}
+  float m0, m1, l0, l1;
+  float scale_log2;
+
+  __device__ __forceinline__ static uint32_t sw(uint32_t base, uint32_t off) {
+    const uint32_t r = off >> 7;
+    return base + (r << 7) + ((((off >> 4) & 7) ^ (r & 7)) << 4) + (off & 15);
+  }
+  __device__ __forceinline__ static uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+  }
+  __device__ __forceinline__ static float4 lds_f4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+  }
+  __device__ __forceinline__ static int4 lds_i4(uint32_t a) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+  }
+
+  __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
+    const int lane = threadIdx.x & 31;
+    const int hg = lane >> 2, q8 = (lane & 3) * 8;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (hg < g) w = *reinterpret_cast<const uint4*>(q_smem + hg * D + 32 * k + q8);
+      qp[4 * k] = w.x;
+      qp[4 * k + 1] = w.y;
+      qp[4 * k + 2] = w.z;
+      qp[4 * k + 3] = w.w;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.0f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.0f;
+    scale_log2 = sl2;
+  }
+
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, q = lane & 3;
+    const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
+
+    // ---- w = q * scale of head gq (channels 32k + 8q + j) and its largest magnitude
+    float w[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 s0 = lds_f4(sw(sb, PG::kOffKs + 4 * (32 * k + 8 * q)));
+      const float4 s1 = lds_f4(sw(sb, PG::kOffKs + 4 * (32 * k + 8 * q) + 16));
+      const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t pr = qp[4 * k + j / 2];
+        w[8 * k + j] = ((j & 1) ? bf16_hi(pr) : bf16_lo(pr)) * sc[j];
+        amax = fmaxf(amax, fabsf(w[8 * k + j]));
+      }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    ex = ex < 1 ? 1 : ex;
+    int sh = 140 - ex;
+    sh = sh < -120 ? -120 : (sh > 120 ? 120 : sh);
+    const float f = __uint_as_float((uint32_t)(127 + sh) << 23);
+    const float finv = __uint_as_float((uint32_t)(127 - sh) << 23);
+
+    float sh_[TT][4], sl_[TT][4];
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sh_[tt][i] = sl_[tt][i] = 0.0f;
+    float bias = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int4 z0 = lds_i4(sw(sb, PG::kOffKz + 4 * (32 * k + 8 * q)));
+      const int4 z1 = lds_i4(sw(sb, PG::kOffKz + 4 * (32 * k + 8 * q) + 16));
+      const int zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+      float ws[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ws[j] = w[8 * k + j] * f;
+        bias = fmaf(ws[j], (float)zz[j], bias);
+      }
+      // k-step 2k: channels +0,+2 | +1,+3 ; k-step 2k+1: +4,+6 | +5,+7
+      uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b0 = 4 * h;
+        bh[h][0] = pack_f16(ws[b0], ws[b0 + 2]);
+        bh[h][1] = pack_f16(ws[b0 + 1], ws[b0 + 3]);
+        const float2 e0 = unpack_f16(bh[h][0]), e1 = unpack_f16(bh[h][1]);
+        bl[h][0] = pack_f16(ws[b0] - e0.x, ws[b0 + 2] - e0.y);
+        bl[h][1] = pack_f16(ws[b0 + 1] - e1.x, ws[b0 + 3] - e1.y);
+      }
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        const int r0 = tt * 16 + gq, r1 = r0 + 8;
+        const uint32_t c0 = lds_u32(sw(sb, PG::kOffK + r0 * ROWB + 16 * k + 4 * q));
+        const uint32_t c1 = lds_u32(sw(sb, PG::kOffK + r1 * ROWB + 16 * k + 4 * q));
+        const uint32_t lo0 = c0 & 0x0F0F0F0Fu, hi0 = (c0 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t lo1 = c1 & 0x0F0F0F0Fu, hi1 = (c1 >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t sel = h ? 0x4342 : 0x4140;
+          uint32_t a[4];
+          a[0] = bytes_to_f16x2(lo0, sel);
+          a[1] = bytes_to_f16x2(lo1, sel);
+          a[2] = bytes_to_f16x2(hi0, sel);
+          a[3] = bytes_to_f16x2(hi1, sel);
+          mma_f16_16816(sh_[tt], a, bh[h][0], bh[h][1]);
+          mma_f16_16816(sl_[tt], a, bl[h][0], bl[h][1]);
+        }
+      }
+    }
+    bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+    bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+    const float bias0 = __shfl_sync(0xffffffffu, bias, 8 * q);
+    const float bias1 = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
+    const float mul0 = __shfl_sync(0xffffffffu, finv, 8 * q) * scale_log2;
+    const float mul1 = __shfl_sync(0xffffffffu, finv, 8 * q + 4) * scale_log2;
+
+    // ---- online softmax for heads 2q, 2q+1
+    float s[TT][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const bool v0 = tt * 16 + gq < valid, v1 = tt * 16 + gq + 8 < valid;
+      s[tt][0] = v0 ? (sh_[tt][0] + sl_[tt][0] - bias0) * mul0 : -INFINITY;
+      s[tt][1] = v0 ? (sh_[tt][1] + sl_[tt][1] - bias1) * mul1 : -INFINITY;
+      s[tt][2] = v1 ? (sh_[tt][2] + sl_[tt][2] - bias0) * mul0 : -INFINITY;
+      s[tt][3] = v1 ? (sh_[tt][3] + sl_[tt][3] - bias1) * mul1 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    uint32_t ph[TT][2], pl[TT][2];
+    float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
+      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      ps0 += p0 + p2;
+      ps1 += p1 + p3;
+      const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
+      const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
+      ph[tt][0] = movmatrix_trans(h01);
+      ph[tt][1] = movmatrix_trans(h23);
+      pl[tt][0] = movmatrix_trans(pack_f16(p0 - f01.x, p1 - f01.y));
+      pl[tt][1] = movmatrix_trans(pack_f16(p2 - f23.x, p3 - f23.y));
+    }
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+    float sum0 = ps0, sum1 = ps1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      sum0 += __shfl_xor_sync(0xffffffffu, sum0, off);
+      sum1 += __shfl_xor_sync(0xffffffffu, sum1, off);
+    }
+    // ---- raw[c][h] = sum_t code_tc p_th, then o = alpha o + scale (raw - zp sum_p)
+#pragma unroll
+    for (int oc = 0; oc < 2; ++oc) {
+      float raw[4][4];
+#pragma unroll
+      for (int sd = 0; sd < 4; ++sd)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[sd][i] = 0.0f;
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        const int t0 = tt * 16 + 2 * q;
+        const uint32_t cb = PG::kOffV + 32 * oc + 4 * gq;
+        const uint32_t W0 = lds_u32(sw(sb, cb + t0 * ROWB));
+        const uint32_t W1 = lds_u32(sw(sb, cb + (t0 + 1) * ROWB));
+        const uint32_t W2 = lds_u32(sw(sb, cb + (t0 + 8) * ROWB));
+        const uint32_t W3 = lds_u32(sw(sb, cb + (t0 + 9) * ROWB));
+        const uint32_t l0w = W0 & 0x0F0F0F0Fu, l1w = W1 & 0x0F0F0F0Fu, l2w = W2 & 0x0F0F0F0Fu, l3w = W3 & 0x0F0F0F0Fu;
+        const uint32_t h0w = (W0 >> 4) & 0x0F0F0F0Fu, h1w = (W1 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t h2w = (W2 >> 4) & 0x0F0F0F0Fu, h3w = (W3 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t x01 = prmt(l0w, l1w, 0x5140), x23 = prmt(l0w, l1w, 0x7362);  // even ch, t0 t1
+        const uint32_t y01 = prmt(h0w, h1w, 0x5140), y23 = prmt(h0w, h1w, 0x7362);  // odd ch, t0 t1
+        const uint32_t z01 = prmt(l2w, l3w, 0x5140), z23 = prmt(l2w, l3w, 0x7362);  // even ch, t2 t3
+        const uint32_t u01 = prmt(h2w, h3w, 0x5140), u23 = prmt(h2w, h3w, 0x7362);  // odd ch, t2 t3
+#pragma unroll
+        for (int sd = 0; sd < 4; ++sd) {
+          const uint32_t sel = (sd & 1) ? 0x4342 : 0x4140;
+          uint32_t A[4];
+          A[0] = bytes_to_f16x2(sd < 2 ? x01 : x23, sel);
+          A[1] = bytes_to_f16x2(sd < 2 ? y01 : y23, sel);
+          A[2] = bytes_to_f16x2(sd < 2 ? z01 : z23, sel);
+          A[3] = bytes_to_f16x2(sd < 2 ? u01 : u23, sel);
+          mma_f16_16816(raw[sd], A, ph[tt][0], ph[tt][1]);
+          mma_f16_16816(raw[sd], A, pl[tt][0], pl[tt][1]);
+        }
+      }
+      const int c0 = 64 * oc + 8 * gq;
+      const float4 s0 = lds_f4(sw(sb, PG::kOffVs + 4 * c0)), s1 = lds_f4(sw(sb, PG::kOffVs + 4 * c0 + 16));
+      const int4 z0 = lds_i4(sw(sb, PG::kOffVz + 4 * c0)), z1 = lds_i4(sw(sb, PG::kOffVz + 4 * c0 + 16));
+      const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const float zf[8] = {(float)z0.x, (float)z0.y, (float)z0.z, (float)z0.w,
+                           (float)z1.x, (float)z1.y, (float)z1.z, (float)z1.w};
+#pragma unroll
+      for (int sd = 0; sd < 4; ++sd) {
+        float* ot = o[4 * oc + sd];
+        const int ce = 2 * sd, co = 2 * sd + 1;  // channels of rows g and g+8
+        ot[0] = fmaf(a0, ot[0], sc[ce] * fmaf(-zf[ce], sum0, raw[sd][0]));
+        ot[1] = fmaf(a1, ot[1], sc[ce] * fmaf(-zf[ce], sum1, raw[sd][1]));
+        ot[2] = fmaf(a0, ot[2], sc[co] * fmaf(-zf[co], sum0, raw[sd][2]));
+        ot[3] = fmaf(a1, ot[3], sc[co] * fmaf(-zf[co], sum1, raw[sd][3]));
+      }
+    }
+  }
+
+  __device__ __forceinline__ void deposit(float* st_acc, float* st_ml) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, q = lane & 3;
+    float s0 = l0, s1 = l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    const int h0 = 2 * q;
+    if (lane < 4) {
+      if (h0 < G) {
+        st_ml[h0 * 2] = m0;
+        st_ml[h0 * 2 + 1] = s0;
+      }
+      if (h0 + 1 < G) {
+        st_ml[(h0 + 1) * 2] = m1;
+        st_ml[(h0 + 1) * 2 + 1] = s1;
+      }
+    }
+#pragma unroll
+    for (int oc = 0; oc < 2; ++oc) {
+#pragma unroll
+      for (int sd = 0; sd < 4; ++sd) {
+        const int c = 64 * oc + 8 * gq + 2 * sd;
+        const float* ot = o[4 * oc + sd];
+        if (h0 < G) {
+          st_acc[h0 * D + c] = ot[0];
+          st_acc[h0 * D + c + 1] = ot[2];
+        }
+        if (h0 + 1 < G) {
+          st_acc[(h0 + 1) * D + c] = ot[1];
+          st_acc[(h0 + 1) * D + c + 1] = ot[3];
+        }
+      }
+    }
+  }
+};
+
 // ------------------------------------------------------------------ the decode kernel
 template <int KV, int D, int BS, int G, int NS, bool TC>
 __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
@@ -884,10 +1171,12 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
   using PG = PageGeom<KV, D, BS>;
   using Cons = typename std::conditional<
       TC,
-      typename std::conditional<KV == PA_KV_BF16, MmaConsumerBf16<D, BS, G>, MmaConsumerU8<BS, G>>::type,
+      typename std::conditional<
+          KV == PA_KV_BF16, MmaConsumerBf16<D, BS, G>,
+          typename std::conditional<KV == PA_KV_UINT8, MmaConsumerU8<BS, G>, MmaConsumerU4<BS, G>>::type>::type,
       FmaConsumer<KV, D, BS, G>>::type;
-  static_assert(!TC || KV == PA_KV_BF16 || (KV == PA_KV_UINT8 && D == 128),
-                "tensor-core consumers: bf16 pages, or uint8 pages of head_dim 128");
+  static_assert(!TC || KV == PA_KV_BF16 || D == 128,
+                "tensor-core consumers: bf16 pages, or quantised pages of head_dim 128");
   constexpr int NST = SM::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled TMA destinations
@@ -1196,7 +1485,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
             const long long page = (long long)phys * Hkv + sg.h;
             issued_n[stage] = n;
             mbar_arrive_expect_tx(&full[stage], PG::kStageBytes);
-            if (TC && KV == PA_KV_UINT8) {
+            if (TC && KV != PA_KV_BF16) {
               // the whole record as one box of 128-byte rows, swizzled
               tma_load_2d(dst, &p.maps.rec, 0, (int)(page * p.maps.rows_per_page), &full[stage], pol);
             } else if (TC) {
@@ -1428,7 +1717,7 @@ cudaError_t dispatch_g(const DecodeParams& prm, const DecodeLaunch& L, cudaStrea
 
 template <int KV, int D, int BS>
 cudaError_t dispatch_path(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
-  if constexpr (KV == PA_KV_BF16 || (KV == PA_KV_UINT8 && D == 128)) {
+  if constexpr (KV == PA_KV_BF16 || D == 128) {
     if (L.tensor_cores) return dispatch_g<KV, D, BS, true>(prm, L, s);
   }
   return dispatch_g<KV, D, BS, false>(prm, L, s);
@@ -1480,7 +1769,7 @@ bool make_pool_maps(int kv_dtype, const PoolDev& pool, PoolMaps& maps) {
                                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill)>(fn);
-  const bool u8 = kv_dtype == PA_KV_UINT8;
+  const bool u8 = kv_dtype != PA_KV_BF16;  // quantised records: rows of 128 bytes
   if (u8 && pool.head_dim != 128) return false;
   const unsigned long long pages = (unsigned long long)pool.num_blocks * pool.num_kv_heads;
   const int rpp = u8 ? (int)(pool.stride / 128) : 2 * pool.block_size;  // rows per record
@@ -1514,7 +1803,8 @@ int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bo
                 : kv_dtype == PA_KV_UINT8
                     ? (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_UINT8, true>(head_dim, block_size, group)
                                                        : smem_bytes_kv<PA_KV_UINT8, false>(head_dim, block_size, group))
-                                          : smem_bytes_kv<PA_KV_UINT4, false>(head_dim, block_size, group);
+                    : (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_UINT4, true>(head_dim, block_size, group)
+                                                       : smem_bytes_kv<PA_KV_UINT4, false>(head_dim, block_size, group));
   const size_t per_sm = 227 * 1024;
   int n = (int)(per_sm / (smem + 1024));
   return n < 1 ? 1 : (n > 4 ? 4 : n);

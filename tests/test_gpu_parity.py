@@ -17,9 +17,9 @@ def _built():
 
 
 def _paths(dt, head_dim=128):
-    """Decode kernels that serve a pool: tensor cores for bf16, and for uint8
-    with head_dim 128; the CUDA-core kernel everywhere."""
-    if dt == "bf16" or (dt == "uint8" and head_dim == 128):
+    """Decode kernels that serve a pool: tensor cores for bf16, and for
+    quantised pools with head_dim 128; the CUDA-core kernel everywhere."""
+    if dt == "bf16" or head_dim == 128:
         return ["cuda_core", "tensor_core"]
     return ["cuda_core"]
 
