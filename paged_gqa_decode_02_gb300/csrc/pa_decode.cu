@@ -84,8 +84,9 @@ struct Smem {
   using PG = PageGeom<KV, D, BS>;
   static constexpr int kStages = W * NS;
   static constexpr int kQBytes = G * D * 2;
-  static constexpr size_t kOffBars = 0;  // full[kStages], empty[kStages], qfull[2], qempty[2]
-  static constexpr size_t kBarBytes = (2 * kStages + 4) * 8;
+  // full[kStages], empty[kStages], qfull[2], qempty[2], deposited, merged
+  static constexpr size_t kOffBars = 0;
+  static constexpr size_t kBarBytes = (2 * kStages + 6) * 8;
   static constexpr size_t kOffFlags = kBarBytes;  // int32 per stage
   static constexpr size_t kOffSegs = (kOffFlags + kStages * 4 + 15) / 16 * 16;
   static constexpr size_t kOffPlan = kOffSegs + kMaxSegs * sizeof(Seg);  // 32 int64
@@ -241,6 +242,24 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total)
   __syncthreads();
   total = tot;
   return x + before;
+}
+
+// ------------------------------------------------------------------ merge stash layout
+//
+// Each consumer warp deposits acc[h][c] of a unit into its stash rows, with
+// the channel index XOR-swizzled so that the deposit's scattered stores hit
+// 32 distinct banks: SWZ 0 keeps channel order (deposits of whole float4 /
+// float2 per lane); SWZ 1 flips channel bits 3-4 by (h >> 1) (bf16 mma
+// fragments: lanes differing in h >> 1 write the same column); SWZ 2 flips
+// bits 0-1 by (h >> 1) (uint8 fragments, columns 4g + 2s); SWZ 3 also folds
+// bit 5 into bit 2 (uint4 fragments, columns 8g + 2s). A lane's four (two)
+// consecutive channels stay within one 16-byte (8-byte) word either way.
+template <int SWZ>
+__device__ __forceinline__ int stash_col(int h, int c) {
+  if constexpr (SWZ == 0) return c;
+  if constexpr (SWZ == 1) return c ^ (((h >> 1) & 3) << 3);
+  if constexpr (SWZ == 2) return c ^ ((h >> 1) & 3);
+  return c ^ ((h >> 1) & 3) ^ (((c >> 5) & 1) << 2);
 }
 
 // ------------------------------------------------------------------ consumer math (CUDA cores)
@@ -411,10 +430,17 @@ struct FmaConsumer {
       st_ml[lane * 2 + 1] = l;
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) st_acc[h * D + lane * CPL + c] = acc[h][c];
+    for (int h = 0; h < G; ++h) {
+      float* dst = st_acc + h * D + lane * CPL;
+      if constexpr (CPL == 4)
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+      else if constexpr (CPL == 2)
+        *reinterpret_cast<float2*>(dst) = make_float2(acc[h][0], acc[h][1]);
+      else
+        for (int c = 0; c < CPL; ++c) dst[c] = acc[h][c];
+    }
   }
+  static constexpr int kStashSwz = 0;
 };
 
 
@@ -589,15 +615,16 @@ struct MmaConsumerBf16 {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       if (h0 < G) {
-        st_acc[h0 * D + mt * 16 + ch] = o[mt][0];
-        st_acc[h0 * D + mt * 16 + ch + 8] = o[mt][2];
+        st_acc[h0 * D + stash_col<1>(h0, mt * 16 + ch)] = o[mt][0];
+        st_acc[h0 * D + stash_col<1>(h0, mt * 16 + ch + 8)] = o[mt][2];
       }
       if (h0 + 1 < G) {
-        st_acc[(h0 + 1) * D + mt * 16 + ch] = o[mt][1];
-        st_acc[(h0 + 1) * D + mt * 16 + ch + 8] = o[mt][3];
+        st_acc[(h0 + 1) * D + stash_col<1>(h0 + 1, mt * 16 + ch)] = o[mt][1];
+        st_acc[(h0 + 1) * D + stash_col<1>(h0 + 1, mt * 16 + ch + 8)] = o[mt][3];
       }
     }
   }
+  static constexpr int kStashSwz = 1;
 };
 
 
@@ -862,16 +889,17 @@ struct MmaConsumerU8 {
         const int c = 32 * pr + 4 * gq + 2 * sd;
         const float* ot = o[2 * pr + sd];
         if (h0 < G) {
-          st_acc[h0 * D + c] = ot[0];
-          st_acc[h0 * D + c + 1] = ot[2];
+          st_acc[h0 * D + stash_col<2>(h0, c)] = ot[0];
+          st_acc[h0 * D + stash_col<2>(h0, c + 1)] = ot[2];
         }
         if (h0 + 1 < G) {
-          st_acc[(h0 + 1) * D + c] = ot[1];
-          st_acc[(h0 + 1) * D + c + 1] = ot[3];
+          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c)] = ot[1];
+          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c + 1)] = ot[3];
         }
       }
     }
   }
+  static constexpr int kStashSwz = 2;
 };
 
 
@@ -1149,24 +1177,83 @@ struct MmaConsumerU4 {
         const int c = 64 * oc + 8 * gq + 2 * sd;
         const float* ot = o[4 * oc + sd];
         if (h0 < G) {
-          st_acc[h0 * D + c] = ot[0];
-          st_acc[h0 * D + c + 1] = ot[2];
+          st_acc[h0 * D + stash_col<3>(h0, c)] = ot[0];
+          st_acc[h0 * D + stash_col<3>(h0, c + 1)] = ot[2];
         }
         if (h0 + 1 < G) {
-          st_acc[(h0 + 1) * D + c] = ot[1];
-          st_acc[(h0 + 1) * D + c + 1] = ot[3];
+          st_acc[(h0 + 1) * D + stash_col<3>(h0 + 1, c)] = ot[1];
+          st_acc[(h0 + 1) * D + stash_col<3>(h0 + 1, c + 1)] = ot[3];
         }
       }
     }
   }
+  static constexpr int kStashSwz = 3;
 };
 
 // ------------------------------------------------------------------ the decode kernel
+// One warp merges the W consumer warps' states of a unit from the stash
+// (M = max_w m_w, f_w = 2^(m_w - M), o = sum_w f_w acc_w / sum_w f_w l_w) and
+// writes heads 0..g-1 to o_dst ([g][D]) and, for a partial, their log-sum-exps
+// (base 2) to lse_dst. Lane j owns channels j*D/32 .. (j+1)*D/32 - 1. All G
+// heads are computed without branches (rows of heads >= g hold stale values
+// and are not stored), so the loads and exponentials of every head overlap.
+// Not inlined: the decode loop keeps its registers.
+template <int D, int G, int W, int SWZ>
+__device__ __noinline__ void merge_stash_warp(const float* __restrict__ st_acc,
+                                              const float* __restrict__ st_ml, int g,
+                                              float* __restrict__ o_dst, float* __restrict__ lse_dst) {
+  constexpr int CPL = D / 32;
+  static_assert(CPL == 2 || CPL == 4, "head_dim 64 or 128");
+  static_assert(SWZ < 2 || CPL == 4, "swizzles of bits 0-2 need four channels per lane");
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float mw[W];
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      mw[w] = st_ml[(w * G + h) * 2];
+      M = fmaxf(M, mw[w]);
+    }
+    float Lsum = 0.0f, A[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) A[c] = 0.0f;
+    // the word holding this lane's channels; SWZ 2 and 3 permute the four
+    // channels inside it by (h >> 1) & 3
+    const int col = stash_col<SWZ>(h, lane * CPL) & ~(CPL - 1);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float f = mw[w] == -INFINITY ? 0.0f : exp2f(mw[w] - M);
+      Lsum = fmaf(st_ml[(w * G + h) * 2 + 1], f, Lsum);
+      const float* src = st_acc + (w * G + h) * D + col;
+      if constexpr (CPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) A[c] = fmaf(x[SWZ >= 2 ? (c ^ ((h >> 1) & 3)) : c], f, A[c]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        A[0] = fmaf(v.x, f, A[0]);
+        A[1] = fmaf(v.y, f, A[1]);
+      }
+    }
+    if (h < g) {
+      const float inv = Lsum > 0.0f ? __frcp_rn(Lsum) : 0.0f;
+      float* dst = o_dst + h * D + lane * CPL;
+      if constexpr (CPL == 4)
+        *reinterpret_cast<float4*>(dst) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
+      else
+        *reinterpret_cast<float2*>(dst) = make_float2(A[0] * inv, A[1] * inv);
+      if (lse_dst != nullptr && lane == 0) lse_dst[h] = Lsum > 0.0f ? M + log2f(Lsum) : -INFINITY;
+    }
+  }
+}
+
 template <int KV, int D, int BS, int G, int NS, bool TC>
-__global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
+__global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     paged_gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kConsumerWarps = consumer_warps<KV, TC, BS>();
-  constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  constexpr int kThreads = (kConsumerWarps + 2) * 32;  // producer, consumers, merger
   using SM = Smem<KV, D, BS, G, NS, kConsumerWarps, TC>;
   using PG = PageGeom<KV, D, BS>;
   using Cons = typename std::conditional<
@@ -1185,6 +1272,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
   uint64_t* empty = full + NST;
   uint64_t* qfull = empty + NST;
   uint64_t* qempty = qfull + 2;
+  uint64_t* deposited = qempty + 2;  // every consumer warp has stashed the unit
+  uint64_t* merged = deposited + 1;   // the merger has read the stash (free again)
   int32_t* stage_flag = reinterpret_cast<int32_t*>(smem + SM::kOffFlags);
   Seg* segs = reinterpret_cast<Seg*>(smem + SM::kOffSegs);
   long long* plan = reinterpret_cast<long long*>(smem + SM::kOffPlan);
@@ -1203,7 +1292,6 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
   __shared__ volatile int abort_flag;
   __shared__ int issued_n[NST];  // last fill issued per stage (drain on abort)
   __shared__ int q_issued[2];    // last q segment index issued per slot
-  __shared__ int merge_flag;
 
   // Launched with programmatic stream serialization: let the combine kernel
   // be scheduled early; write no global memory and read no page before the
@@ -1228,6 +1316,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], kConsumerWarps);
     }
+    mbar_init(deposited, kConsumerWarps);
+    mbar_init(merged, 1);
     abort_flag = 0;
     q_issued[0] = q_issued[1] = -1;
     fence_mbar_init();
@@ -1239,6 +1329,12 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
   // window's segment list.
   int* lens_sm = reinterpret_cast<int*>(stash_acc);
   constexpr int kLensSmem = (int)(SM::kStashAccBytes / 4);
+  // With at most one sequence per thread (the usual case) one block scan
+  // gives every sequence's first page, so the slice start and the prefix
+  // CTA 0 publishes need no second pass over the lengths.
+  const bool one_pass = p.batch <= kThreads;
+  if (tid == 0) plan[0] = -1;
+  int my_pages = 0, my_incl = 0;
   long long npages_all = 0;
   {
     int part = 0;
@@ -1248,15 +1344,20 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
       part += (len + BS - 1) / BS;
     }
     int tot;
-    block_incl_scan(part, warp_tot, tot);
+    my_incl = block_incl_scan(part, warp_tot, tot);
+    my_pages = part;
     npages_all = tot;
   }
   const long long T = npages_all * Hkv;
   const long long s_i = T * cta / Gc, e_i = T * (cta + 1) / Gc;
-  // CTA 0 publishes the per-sequence prefix for the combine kernel; every
-  // CTA finds the sequence holding its first page.
-  if (tid == 0) plan[0] = -1;
-  {
+  // every thread block finds the sequence holding its first page
+  if (one_pass) {
+    const long long lo = (long long)(my_incl - my_pages) * Hkv, hi = (long long)my_incl * Hkv;
+    if (tid < p.batch && s_i >= lo && s_i < hi) {
+      plan[0] = tid;
+      plan[1] = lo;
+    }
+  } else {
     int running = 0;
     for (int base = 0; base < p.batch; base += kThreads) {
       const int b = base + tid;
@@ -1290,15 +1391,20 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
       waited = true;
     }
     if (cta != 0) return;
-    int running = 0;
-    for (int base = 0; base < p.batch; base += kThreads) {
-      const int b = base + tid;
-      const int n = b < p.batch ? ((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS : 0;
-      int tot;
-      const int incl = block_incl_scan(n, warp_tot, tot);
-      if (b < p.batch) p.pre_pages[b] = running + incl - n;
-      if (b == p.batch - 1) p.pre_pages[p.batch] = running + incl;
-      running += tot;
+    if (one_pass) {
+      if (tid < p.batch) p.pre_pages[tid] = my_incl - my_pages;
+      if (tid == p.batch - 1) p.pre_pages[p.batch] = my_incl;
+    } else {
+      int running = 0;
+      for (int base = 0; base < p.batch; base += kThreads) {
+        const int b = base + tid;
+        const int n = b < p.batch ? ((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS : 0;
+        int tot;
+        const int incl = block_incl_scan(n, warp_tot, tot);
+        if (b < p.batch) p.pre_pages[b] = running + incl - n;
+        if (b == p.batch - 1) p.pre_pages[p.batch] = running + incl;
+        running += tot;
+      }
     }
     if (p.batch == 0 && tid == 0) p.pre_pages[0] = 0;
     if (p.fused) {
@@ -1325,6 +1431,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
   bool lens_cached = true;  // lens_sm valid until the first merge overwrites the stash
   uint64_t pol = policy_evict_first();
   Cons cons;  // consumer warps' online-softmax state; persists across windows
+  int n_dep = 0;  // units this warp has deposited (phase of `merged` to wait for)
 
   while (pos < e_i) {
     // ---- build this window's segment list (warp 0)
@@ -1413,17 +1520,37 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
     cur_base = plan[5];
     const int kw0 = (int)(pos - s_i), kw1 = (int)(wend - s_i);
 
-    if (warp == 0) {
-      // (1) the window's block-table entries -> shared memory, all lanes
-      int sx = 0;
-      for (int i = lane; i < kw1 - kw0; i += 32) {
-        const int k = kw0 + i;
-        while (sx + 1 < nseg && k >= segs[sx + 1].k0) ++sx;
-        const Seg& sg = segs[sx];
-        phys_s[i] = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
+    {
+      // the window's block-table entries -> shared memory, by every thread,
+      // kStageLoads independent loads in flight per thread (one round trip
+      // for windows of up to kStageLoads * kThreads pages)
+      constexpr int kStageLoads = 4;
+      const int nwin = kw1 - kw0;
+      for (int i0 = 0; i0 < nwin; i0 += kStageLoads * kThreads) {
+        int v[kStageLoads];
+#pragma unroll
+        for (int u = 0; u < kStageLoads; ++u) {
+          const int i = i0 + u * kThreads + tid;
+          v[u] = 0;
+          if (i < nwin) {
+            const int k = kw0 + i;
+            int lo = 0, hi = nseg - 1;  // last segment starting at or before k
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (segs[mid].k0 <= k) lo = mid; else hi = mid - 1;
+            }
+            const Seg& sg = segs[lo];
+            v[u] = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kStageLoads; ++u) {
+          const int i = i0 + u * kThreads + tid;
+          if (i < nwin) phys_s[i] = v[u];
+        }
       }
-      __syncwarp();
     }
+    __syncthreads();
     wait_and_publish();  // first window only: pages and outputs follow
 
     if (warp == 0) {
@@ -1436,31 +1563,51 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
       // phases behind, take its parity for "released" and overwrite a stage
       // still in use.) A sub-batch never crosses the start of a segment: the
       // segment's q goes out first (lane 0).
-      int qseg = 0;
+      // q of segment qi into its slot (lane 0). The slot is free once every
+      // consumer warp has begun segment qi - 2; without `block` the copy is
+      // only sent if it already is.
+      auto send_q = [&](int qi, bool block) -> bool {
+        const int gs = seg_counter + qi;
+        const int slot = gs & 1;
+        if (gs >= 2 && !abort_flag) {
+          const uint32_t par = ((gs >> 1) - 1) & 1;
+          if (!block) {
+            if (!mbar_try_wait(&qempty[slot], par)) return false;
+          } else if (!mbar_wait_bounded(&qempty[slot], par)) {
+            set_error(p.pool.err, PA_DEVERR_TIMEOUT);
+            abort_flag = 1;
+          }
+        }
+        const Seg& qs = segs[qi];
+        const uint16_t* qsrc = p.q + ((long long)qs.b * p.num_q_heads + (long long)qs.h * g) * D;
+        if (abort_flag) {
+          mbar_arrive(&qfull[slot]);
+        } else {
+          q_issued[slot] = gs;
+          mbar_arrive_expect_tx(&qfull[slot], g * D * 2);
+          bulk_g2s(qslots + slot * SM::kQBytes, qsrc, g * D * 2, &qfull[slot], pol);
+        }
+        return true;
+      };
+      // the window's q rows -> L2 now, so that a q sent late still lands fast
+      for (int qi = lane; qi < nseg; qi += 32) {
+        const uint16_t* qsrc = p.q + ((long long)segs[qi].b * p.num_q_heads + (long long)segs[qi].h * g) * D;
+        prefetch_l2_bulk(qsrc, g * D * 2);
+      }
+      int qseg = 0;    // segments whose first page the issue has reached
+      int q_sent = 0;  // segments whose q has been sent (lane 0's count)
       for (int k = kw0; k < kw1;) {
         if (qseg < nseg && segs[qseg].k0 == k) {
-          if (lane == 0) {
-            const int gs = seg_counter + qseg;
-            const int slot = gs & 1;
-            bool ok = true;
-            if (gs >= 2 && !abort_flag) ok = mbar_wait_bounded(&qempty[slot], ((gs >> 1) - 1) & 1);
-            if (!ok) {
-              set_error(p.pool.err, PA_DEVERR_TIMEOUT);
-              abort_flag = 1;
-            }
-            const Seg& qs = segs[qseg];
-            const uint16_t* qsrc = p.q + ((long long)qs.b * p.num_q_heads + (long long)qs.h * g) * D;
-            if (abort_flag) {
-              mbar_arrive(&qfull[slot]);
-            } else {
-              q_issued[slot] = gs;
-              mbar_arrive_expect_tx(&qfull[slot], g * D * 2);
-              bulk_g2s(qslots + slot * SM::kQBytes, qsrc, g * D * 2, &qfull[slot], pol);
-            }
+          if (lane == 0 && q_sent == qseg) {
+            send_q(qseg, true);
+            ++q_sent;
           }
           ++qseg;
           __syncwarp();
         }
+        // the next segment's q goes out as soon as its slot is free, a ring's
+        // worth of pages before the consumers need it
+        if (lane == 0 && q_sent == qseg && q_sent < nseg && send_q(q_sent, false)) ++q_sent;
         int kend = min(kw1, k + (NST < 32 ? NST : 32));
         if (qseg < nseg) kend = min(kend, segs[qseg].k0);
         const int kk = k + lane;
@@ -1503,10 +1650,19 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
         __syncwarp();
         k = kend;
       }
-    } else {
+    } else if (warp <= kConsumerWarps) {
       // ---------------------------------------------------------- consumers
       const int cw = warp - 1;
       float* pbuf = pbuf_all + cw * BS * G;
+      if (pos == s_i) {
+        // warm the instruction cache while the first pages are in flight: the
+        // deposit runs once per unit, and its first run would otherwise fetch
+        // instructions mid-stream, with memory saturated. A dry run into this
+        // warp's own stash rows (free: the planning is done with them).
+        Cons dry;
+        dry.begin_unit(reinterpret_cast<const uint16_t*>(qslots), g, p.scale_log2);
+        dry.deposit(stash_acc + cw * G * D, stash_ml + cw * G * 2);
+      }
       for (int si = 0; si < nseg; ++si) {
         const Seg sg = segs[si];
         const int gs = seg_counter + si;
@@ -1539,37 +1695,53 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
           if (lane == 0) mbar_arrive(&empty[stage]);
         }
         if (sg.flags & kContNext) continue;  // the run goes on in the next window
-        cons.deposit(stash_acc + cw * G * D, stash_ml + cw * G * 2);
-        named_bar_sync(1, kConsumerWarps * 32);
-        // ---- merge the warps' states and write
-        const int ctid = tid - 32;
-        const long long row0 = (long long)sg.b * p.num_q_heads + (long long)sg.h * g;
-        for (int e = ctid; e < g * D; e += kConsumerWarps * 32) {
-          const int h = e / D, c = e % D;
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stash_ml[(w * G + h) * 2]);
-          float Lsum = 0.0f, A = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = stash_ml[(w * G + h) * 2];
-            const float f = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-            Lsum += stash_ml[(w * G + h) * 2 + 1] * f;
-            A += stash_acc[(w * G + h) * D + c] * f;
-          }
-          const float o = Lsum > 0.0f ? A / Lsum : 0.0f;
-          if (sg.slot < 0) {
-            p.out[(row0 + h) * D + c] = o;
-          } else {
-            p.part_o[((long long)sg.slot * g + h) * D + c] = o;
-            if (c == 0) p.part_lse[(long long)sg.slot * g + h] = Lsum > 0.0f ? M + log2f(Lsum) : -INFINITY;
+        // ---- hand this warp's state of the unit to the merger warp and go on
+        // with the next unit's pages (waiting for the other warps here would
+        // idle every warp until the unit's slowest page had landed and been
+        // merged, and the ring would run dry)
+        if (n_dep > 0) {
+          // the stash is free once the previous unit's merge has read it
+          const bool okm = mbar_wait_bounded(merged, (n_dep - 1) & 1);
+          if (!okm && abort_flag == 0) {
+            if (lane == 0) set_error(p.pool.err, PA_DEVERR_TIMEOUT);
+            abort_flag = 1;
           }
         }
+        ++n_dep;
+        cons.deposit(stash_acc + cw * G * D, stash_ml + cw * G * 2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(deposited);  // release: the stash rows above
+      }
+    } else {
+      // ---------------------------------------------------------- merger
+      // One warp merges each finished unit from the stash (in segment order,
+      // as the consumers deposit them) and writes its row or partial.
+      if (pos == s_i) {
+        // instruction-cache warm-up while the first pages are in flight: a
+        // dry merge that stores nothing (no heads); what it reads is discarded
+        merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, 0, p.out, nullptr);
+      }
+      for (int si = 0; si < nseg; ++si) {
+        const Seg sg = segs[si];
+        if (sg.flags & kContNext) continue;
+        const bool okd = mbar_wait_bounded(deposited, n_dep & 1);
+        if (!okd && abort_flag == 0) {
+          if (lane == 0) set_error(p.pool.err, PA_DEVERR_TIMEOUT);
+          abort_flag = 1;
+        }
+        ++n_dep;
+        const long long row0 = (long long)sg.b * p.num_q_heads + (long long)sg.h * g;
+        if (sg.slot < 0)
+          merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.out + row0 * D, nullptr);
+        else
+          merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.part_o + (long long)sg.slot * g * D,
+                                                                  p.part_lse + (long long)sg.slot * g);
         if (sg.slot >= 0 && p.fused) {
           // the last slice to finish this unit merges its partials (threadfence
-          // reduction: partials are fenced before the ticket is taken)
+          // reduction: partials are fenced before the ticket is taken); the
+          // stash, read out above, is the scratch
           __threadfence();
-          named_bar_sync(1, kConsumerWarps * 32);
+          __syncwarp();
           UnitSlices usl;
           usl.n = (sg.len + BS - 1) / BS;
           usl.us = s_i + sg.k0 - sg.lp0;
@@ -1578,7 +1750,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
           usl.first = owner_of(usl.us, T, Gc);
           usl.last = owner_of(usl.us + usl.n - 1, T, Gc);
           const long long u = (long long)sg.b * Hkv + sg.h;
-          if (ctid == 0) {
+          int last_slice = 0;
+          if (lane == 0) {
             const unsigned long long tag = p.epoch << 24;
             unsigned long long* t = p.tickets + u;
             unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(t), assumed;
@@ -1589,17 +1762,17 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 1) * 32, 1)
               mine = done + 1;
               old = atomicCAS(t, assumed, tag | mine);
             } while (old != assumed);
-            merge_flag = mine == (unsigned long long)usl.count() ? 1 : 0;
+            last_slice = mine == (unsigned long long)usl.count() ? 1 : 0;
           }
-          named_bar_sync(1, kConsumerWarps * 32);
-          if (merge_flag) {
+          last_slice = __shfl_sync(0xffffffffu, last_slice, 0);
+          if (last_slice) {
             __threadfence();
-            merge_unit_partials<D>(usl, u, row0, g, p.part_o, p.part_lse, p.out, ctid,
-                                   kConsumerWarps * 32, stash_acc,
-                                   [] { named_bar_sync(1, kConsumerWarps * 32); });
+            merge_unit_partials<D>(usl, u, row0, g, p.part_o, p.part_lse, p.out, lane, 32, stash_acc,
+                                   [] { __syncwarp(); });
           }
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merged);  // the stash may be overwritten
       }
     }
     seg_counter += nseg;
@@ -1669,7 +1842,7 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.num_ctas);
-  cfg.blockDim = dim3((consumer_warps<KV, TC, BS>() + 1) * 32);
+  cfg.blockDim = dim3((consumer_warps<KV, TC, BS>() + 2) * 32);
   cfg.dynamicSmemBytes = SM::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
