@@ -132,12 +132,12 @@ PA_API pa_status pa_append_kv(pa_pool* pool, const void* k_new, const void* v_ne
 
 /* pa_decode: one decode step of grouped-query attention over the paged pool
  * (engine article section 4.3; TFFInfer section 3.7.2 online softmax).
- *   q            device bf16 [batch][num_q_heads][head_dim]
+ *   q            device bf16 [batch][num_q_heads][head_dim], 16-byte aligned
  *   block_table  device int32 [batch][max_blocks]
  *   seq_lens     device int32 [batch]: tokens to attend (the step's new token
  *                already appended); 0 gives a zero output row
  *   softmax_scale usually 1/sqrt(head_dim)
- *   out          device float32 [batch][num_q_heads][head_dim]
+ *   out          device float32 [batch][num_q_heads][head_dim], 16-byte aligned
  *   workspace    device scratch of at least pa_decode_workspace_bytes(...)
  *                bytes (256-byte aligned), caller-owned. Zero it once after
  *                allocating it: a small part holds merge tickets tagged with

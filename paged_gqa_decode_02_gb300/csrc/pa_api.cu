@@ -290,8 +290,8 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   if (batch == 0) return PA_OK;
   if (!q || !block_table || !seq_lens || !out || !workspace || max_blocks == 0)
     return fail(PA_ERR_INVALID_ARG, "null device pointer or max_blocks == 0%s");
-  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return fail(PA_ERR_INVALID_ARG, "q must be 16-byte aligned and workspace 256-byte aligned%s");
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned and workspace 256-byte aligned%s");
   const int ctas = num_splits > 0 ? num_splits : auto_splits(p, group);
   const size_t need = pa::decode_workspace_bytes(ctas, batch, p->desc.num_kv_heads, group,
                                                  p->desc.head_dim);

@@ -1795,36 +1795,140 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
 // were written by the decode kernel; empty sequences get zero rows; the rest
 // merge their partials: M = max_s lse_s, w_s = 2^(lse_s - M),
 // out = sum_s w_s o_s / sum_s w_s (the same algebra as the online-softmax
-// update, applied to whole partial states). The log-sum-exps of up to 32
-// slices are staged in shared memory with one round of loads.
+// update, applied to whole partial states).
+//
+// Everything that depends only on the lengths (the unit's page range, its
+// slices and which of them hold a partial) is worked out before the wait on
+// the decode kernel when the caller allows reading the lengths early (they
+// are inputs the decode kernel never writes); after the wait one round of
+// loads fetches every partial of the unit: a thread owns four channels of
+// one head and issues its loads for all slices back to back.
 template <int D>
 __global__ void __launch_bounds__(256)
-    splitkv_combine_kernel(const int32_t* pre_pages, const float* part_o, const float* part_lse,
-                           float* out, int batch, int num_kv_heads, int group, int num_q_heads,
-                           int num_ctas) {
-  __shared__ float wgt[32 * 8 + 8];
+    splitkv_combine_kernel(const int32_t* seq_lens, const int32_t* pre_pages, const float* part_o,
+                           const float* part_lse, float* out, int batch, int num_kv_heads, int group,
+                           int num_q_heads, int num_ctas, int block_size, int max_blocks, int lens_early) {
+  constexpr int kMaxSl = 64;  // slices handled from the precomputed mask; more go round again
+  __shared__ long long sh_sum[2][8];
   pdl_launch_dependents();
-  pdl_wait();
-  const int u = blockIdx.x, tid = threadIdx.x;
+  const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = u / num_kv_heads, j = u % num_kv_heads;
-  const long long pre = pre_pages[b];
-  const long long n = pre_pages[b + 1] - pre;
-  const long long T = (long long)pre_pages[batch] * num_kv_heads;
+  long long pre = 0, n = 0, T = 0;
+  auto unit_range = [&](bool from_lens) {
+    if (from_lens) {
+      // pages of every sequence and of those before b, from the lengths
+      // (invalid lengths count as empty, as in the decode kernel)
+      long long all = 0, before = 0;
+      for (int x = tid; x < batch; x += blockDim.x) {
+        const int len = seq_lens[x];
+        const long long np =
+            (len < 0 || (long long)len > (long long)max_blocks * block_size) ? 0 : (len + block_size - 1) / block_size;
+        all += np;
+        if (x < b) before += np;
+        if (x == b) n = np;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        all += __shfl_xor_sync(0xffffffffu, all, o);
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+      }
+      if (lane == 0) {
+        sh_sum[0][warp] = all;
+        sh_sum[1][warp] = before;
+      }
+      __syncthreads();
+      all = before = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        all += sh_sum[0][w];
+        before += sh_sum[1][w];
+      }
+      // n: the thread that saw b shares it
+      __syncthreads();
+      if (b % (int)blockDim.x == tid) sh_sum[0][0] = n;
+      __syncthreads();
+      n = sh_sum[0][0];
+      pre = before;
+      T = all * num_kv_heads;
+    } else {
+      pre = pre_pages[b];
+      n = pre_pages[b + 1] - pre;
+      T = (long long)pre_pages[batch] * num_kv_heads;
+    }
+  };
+  UnitSlices usl;
+  unsigned long long mask0 = 0;  // first round's slices that hold a partial
+  auto unit_slices = [&]() {
+    usl.us = pre * num_kv_heads + (long long)j * n;
+    usl.n = n;
+    usl.T = T;
+    usl.G = num_ctas;
+    usl.first = n > 0 ? owner_of(usl.us, T, num_ctas) : 0;
+    usl.last = n > 0 ? owner_of(usl.us + n - 1, T, num_ctas) : 0;
+    const int cnt = (int)min((long long)kMaxSl, usl.last - usl.first + 1);
+    for (int i = 0; i < cnt && usl.first != usl.last; ++i)
+      if (usl.has_part(usl.first + i)) mask0 |= 1ull << i;
+  };
+  if (lens_early) {
+    unit_range(true);
+    unit_slices();
+  }
+  pdl_wait();
+  if (!lens_early) {
+    unit_range(false);
+    unit_slices();
+  }
   const long long row0 = (long long)b * num_q_heads + (long long)j * group;
   if (n == 0) {
     for (int e = tid; e < group * D; e += blockDim.x) out[row0 * D + e] = 0.0f;
     return;
   }
-  UnitSlices usl;
-  usl.us = pre * num_kv_heads + (long long)j * n;
-  usl.n = n;
-  usl.T = T;
-  usl.G = num_ctas;
-  usl.first = owner_of(usl.us, T, num_ctas);
-  usl.last = owner_of(usl.us + n - 1, T, num_ctas);
   if (usl.first == usl.last) return;
-  merge_unit_partials<D>(usl, u, row0, group, part_o, part_lse, out, tid, blockDim.x, wgt,
-                         [] { __syncthreads(); });
+  // this thread's four channels of head h
+  const int e0 = tid * 4;
+  if (e0 >= group * D) return;
+  const int h = e0 / D;
+  float M = -INFINITY, W = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (long long s0 = usl.first; s0 <= usl.last; s0 += kMaxSl) {
+    const int cnt = (int)min((long long)kMaxSl, usl.last - s0 + 1);
+    // slices of this round holding a partial (block-uniform)
+    unsigned long long mask = mask0;
+    if (s0 != usl.first) {
+      mask = 0;
+      for (int i = 0; i < cnt; ++i)
+        if (usl.has_part(s0 + i)) mask |= 1ull << i;
+    }
+    // one round of loads: lse and four channels of every partial
+    constexpr int kBatch = 8;
+    for (int i0 = 0; i0 < cnt; i0 += kBatch) {
+      float l[kBatch];
+      float4 o[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + k;
+        l[k] = -INFINITY;
+        o[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (i < cnt && ((mask >> i) & 1)) {
+          const long long slot = s0 + i + u;
+          l[k] = __ldcg(part_lse + slot * group + h);
+          o[k] = __ldcg(reinterpret_cast<const float4*>(part_o + slot * group * D + e0));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (l[k] == -INFINITY) continue;
+        const float Mn = fmaxf(M, l[k]);
+        const float a = M == -INFINITY ? 0.0f : exp2f(M - Mn), w = exp2f(l[k] - Mn);
+        W = W * a + w;
+        A[0] = A[0] * a + w * o[k].x;
+        A[1] = A[1] * a + w * o[k].y;
+        A[2] = A[2] * a + w * o[k].z;
+        A[3] = A[3] * a + w * o[k].w;
+        M = Mn;
+      }
+    }
+  }
+  const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+  *reinterpret_cast<float4*>(out + row0 * D + e0) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
 }
 
 template <int KV, int D, int BS, int G, int NS, bool TC>
@@ -1854,10 +1958,10 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   cfg.gridDim = dim3(units);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D>, (const int32_t*)prm.pre_pages,
-                            (const float*)prm.part_o, (const float*)prm.part_lse, prm.out,
-                            prm.batch, prm.pool.num_kv_heads, prm.group, prm.num_q_heads,
-                            L.num_ctas);
+  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D>, prm.seq_lens, (const int32_t*)prm.pre_pages,
+                            (const float*)prm.part_o, (const float*)prm.part_lse, prm.out, prm.batch,
+                            prm.pool.num_kv_heads, prm.group, prm.num_q_heads, L.num_ctas, prm.pool.block_size,
+                            prm.max_blocks, prm.early_plan);
 }
 
 // Stages per consumer warp: as many pages in flight as the shared memory

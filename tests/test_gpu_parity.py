@@ -122,6 +122,12 @@ def test_host_validation_errors():
     with pytest.raises(B.PagedAttnError) as e:
         g.decode(q, H.dev(wl.block_table), H.dev(wl.seq_lens), 0.125, workspace=ws)
     assert e.value.status == 3
+    # out must be 16-byte aligned (rows are written as float4)
+    n = wl.batch * wl.num_q_heads * wl.head_dim
+    out_off = torch.empty(n + 1, dtype=torch.float32, device="cuda")[1:].view(wl.batch, wl.num_q_heads, wl.head_dim)
+    with pytest.raises(B.PagedAttnError) as e:
+        g.decode(q, H.dev(wl.block_table), H.dev(wl.seq_lens), 0.125, out=out_off)
+    assert e.value.status == 1 and "16-byte" in str(e.value)
 
 
 FULL = ["qwen25_7b_bf16", "qwen3_8b_int8", "long_uint4", "prefix_mix"]
@@ -164,17 +170,18 @@ def test_slices_longer_than_a_window(dt):
     assert g.device_error() == (0, 0)
 
 
+@pytest.mark.parametrize("early_plan", [False, True])
 @pytest.mark.parametrize("combine", ["fused", "separate"])
 @pytest.mark.parametrize("splits", [0, 300, 2000])
-def test_many_slices_per_sequence(splits, combine):
-    """Units cut into many slices (up to 32 and beyond) with a 7-head group:
-    the merge stages slices x heads log-sum-exps with fewer threads than
-    entries."""
+def test_many_slices_per_sequence(splits, combine, early_plan):
+    """Units cut into many slices (up to 32, and past the combine's 64-slice
+    rounds) with a 7-head group; with early_plan the combine works out each
+    unit's slices from the lengths before waiting on the decode kernel."""
     wl = W.make_case("many_slices", 92, 3, 28, 4, 128, 16, "bf16", [700, 33, 1500], extra_blocks=2)
     g, o = H.load_both(wl)
     ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
     for path in _paths("bf16"):
-        got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine)
-        H.check_attention(got, ref, f"many slices splits={splits} {path} {combine}")
+        got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine, early_plan=early_plan)
+        H.check_attention(got, ref, f"many slices splits={splits} {path} {combine} early={early_plan}")
     assert g.device_error() == (0, 0)
