@@ -166,6 +166,7 @@ def run_ours(args):
     pool = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, local)
     pool.set_decode_path(args.path, fused_combine=(args.combine == "fused"),
                          early_plan=not args.no_early_plan)
+    pool.set_unit_cost(args.unit_cost)
 
     def d(a):
         a = np.ascontiguousarray(a)
@@ -292,6 +293,7 @@ def run_ours(args):
                            + args.combine + ")",
                    "decode_path": args.path,
                    "early_plan": not args.no_early_plan,
+                   "unit_cost": args.unit_cost,
                    "l2": "flushed before every timed step (256 MiB write, outside the event brackets)",
                    "parallelism": f"replicas x{world} (no exchange)"},
         "hbm_gbs": achieved,
@@ -398,6 +400,8 @@ def main():
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core"])
     ap.add_argument("--combine", default="separate", choices=["fused", "separate"])
+    ap.add_argument("--unit-cost", type=int, default=-1,
+                    help="phantom pages per unit in the cost-balanced partition (-1: the library default)")
     ap.add_argument("--no-early-plan", action="store_true",
                     help="decode plans only after the append kernel has finished")
     ap.add_argument("--cpu-seqs", type=int, default=1 << 30)

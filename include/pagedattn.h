@@ -196,8 +196,10 @@ PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
  * PA_DECODE_EARLY_PLAN lets the decode kernel read seq_lens and block_table
  * (and plan its work) while the kernel launched just before it on the stream
  * is still running; it still waits for that kernel before reading any page or
- * writing anything. Set it only when that preceding kernel writes neither
- * seq_lens nor block_table (pa_append_kv writes neither).
+ * writing anything; the split-KV combine kernel likewise reads seq_lens
+ * before waiting on the decode kernel. Set it only when that preceding
+ * kernel writes neither seq_lens nor block_table (pa_append_kv writes
+ * neither).
  * PA_ERR_UNSUPPORTED if TENSOR_CORE is asked for a pool it does not serve. */
 typedef enum {
   PA_DECODE_AUTO = 0,
@@ -207,6 +209,17 @@ typedef enum {
   PA_DECODE_EARLY_PLAN = 8
 } pa_decode_path;
 PA_API pa_status pa_pool_set_decode_path(pa_pool* pool, int32_t path);
+
+/* Partition of a pool's decode work: the thread blocks take equal shares of
+ * a line on which each (sequence, kv head) unit occupies its pages plus
+ * `unit_cost_pages` more positions, standing for the fixed work of a unit
+ * (loading its query, merging the warps' states, writing its row or
+ * partial) in units of page time. A block whose share crosses many unit
+ * boundaries thus gets fewer pages. 0 splits the pages evenly; a negative
+ * value restores the default of the pool's decode kernel. The results do
+ * not depend on it. PA_ERR_INVALID_ARG for a null pool or a value above
+ * 4096. */
+PA_API pa_status pa_pool_set_unit_cost(pa_pool* pool, int32_t unit_cost_pages);
 
 /* Device addresses of the pool's arrays, for inspection and tests. */
 PA_API pa_status pa_pool_view(const pa_pool* pool, pa_pool_buffers* out);

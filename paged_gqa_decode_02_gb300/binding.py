@@ -75,6 +75,8 @@ def lib():
         L.pa_decode_workspace_bytes.restype = SZ
         L.pa_pool_set_decode_path.argtypes = [P, I32]
         L.pa_pool_set_decode_path.restype = I32
+        L.pa_pool_set_unit_cost.argtypes = [P, I32]
+        L.pa_pool_set_unit_cost.restype = I32
         L.pa_decode_num_splits.argtypes = [P, I32]
         L.pa_decode_num_splits.restype = I32
         L.pa_pool_view.argtypes = [P, ctypes.POINTER(pa_pool_buffers)]
@@ -144,6 +146,10 @@ DECODE_PATHS = {"auto": 0, "cuda_core": 1, "tensor_core": 2}
 
 def pa_pool_set_decode_path(handle, path):
     _check(lib().pa_pool_set_decode_path(handle, DECODE_PATHS[path] if isinstance(path, str) else int(path)))
+
+
+def pa_pool_set_unit_cost(handle, unit_cost_pages):
+    _check(lib().pa_pool_set_unit_cost(handle, int(unit_cost_pages)))
 
 
 def pa_decode_num_splits(handle, num_splits=0):
@@ -230,6 +236,11 @@ class PagedKVPool:
         code |= PA_DECODE_FUSED_COMBINE if fused_combine else 0
         code |= PA_DECODE_EARLY_PLAN if early_plan else 0
         pa_pool_set_decode_path(self.handle, code)
+
+    def set_unit_cost(self, unit_cost_pages=-1):
+        """Phantom pages per (sequence, kv head) unit in the decode's
+        cost-balanced partition (see pa_pool_set_unit_cost); -1 = default."""
+        pa_pool_set_unit_cost(self.handle, unit_cost_pages)
 
     def workspace_bytes(self, batch, num_q_heads, num_splits=0):
         return pa_decode_workspace_bytes(self.handle, batch, num_q_heads, num_splits)

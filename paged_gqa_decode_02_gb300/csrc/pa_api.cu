@@ -17,6 +17,7 @@ struct pa_pool {
   int32_t decode_path;
   bool fused_combine;
   bool early_plan;
+  int32_t unit_cost;  // partition: phantom pages per unit; < 0 = the kernel's default
   void* slab;
   size_t slab_bytes;
   pa::PoolDev dev;
@@ -72,6 +73,15 @@ struct DeviceGuard {
     if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
   }
 };
+
+// Default phantom pages per unit of the cost-balanced partition: the fixed
+// work of a unit (query load, state deposit and merge, row or partial write)
+// in page times of the pool's decode kernel, as measured on GB300 over the
+// Qwen-shaped bf16 and uint8 workloads and the prefix-sharing mix (uint8
+// pages are short to stream and costly to decode, so a unit weighs more).
+int32_t default_unit_cost(const pa_pool* p) {
+  return p->desc.kv_dtype == PA_KV_UINT8 ? 10 : 6;
+}
 
 bool uses_tensor_cores(const pa_pool* p) {
   return p->maps.valid && p->decode_path != PA_DECODE_CUDA_CORE;
@@ -172,6 +182,7 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   p->decode_path = PA_DECODE_AUTO;
   p->fused_combine = false;
   p->early_plan = false;
+  p->unit_cost = -1;
   p->maps.valid = 0;
   pa::make_pool_maps(d->kv_dtype, p->dev, p->maps);
   *out = p;
@@ -259,6 +270,14 @@ pa_status pa_pool_set_decode_path(pa_pool* p, int32_t path) {
   return PA_OK;
 }
 
+pa_status pa_pool_set_unit_cost(pa_pool* p, int32_t unit_cost_pages) {
+  g_last_error[0] = 0;
+  if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  if (unit_cost_pages > 4096) return fail(PA_ERR_INVALID_ARG, "unit cost above 4096 pages%s");
+  p->unit_cost = unit_cost_pages < 0 ? -1 : unit_cost_pages;
+  return PA_OK;
+}
+
 int32_t pa_decode_num_splits(const pa_pool* p, int32_t num_splits) {
   if (!p || num_splits < 0) return 0;
   return num_splits > 0 ? num_splits : auto_splits(p, 8);
@@ -309,6 +328,7 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   L.fused_combine = p->fused_combine;
   L.early_plan = p->early_plan;
   L.epoch = next_epoch();
+  L.unit_cost = p->unit_cost >= 0 ? p->unit_cost : default_unit_cost(p);
   cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
                                     workspace, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode launch");

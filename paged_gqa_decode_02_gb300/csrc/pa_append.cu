@@ -151,6 +151,9 @@ cudaError_t launch_append_t(const PoolDev& pool, const void* k_new, const void* 
                             const int32_t* cu_new, const int32_t* ctx_lens,
                             const int32_t* block_table, int batch, int max_blocks,
                             int blocks_per_seq, cudaStream_t stream) {
+  static std::atomic<unsigned long long> ready{0};  // per instantiation, per device
+  const cudaError_t e = prepare_kernel(kv_append_kernel<KV, BS>, 0, ready);
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

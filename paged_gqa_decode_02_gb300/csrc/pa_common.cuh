@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -131,6 +132,34 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
 // 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src_gmem, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// Prefetch a TMA descriptor (kernel parameter) into the descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const void* desc) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(desc) : "memory");
+}
+
+// One-time per-device launch set-up of a kernel (host side): its dynamic
+// shared memory limit, and the shared-memory carveout pinned to the maximum.
+// Every kernel of the library uses the same carveout because an SM runs
+// thread blocks of two kernels side by side (as a programmatic dependent
+// launch does with a kernel and the one after it) only while their carveouts
+// agree; otherwise the later kernel's blocks wait for the SM to drain.
+template <typename Kernel>
+inline cudaError_t prepare_kernel(Kernel kern, int dyn_smem_bytes, std::atomic<unsigned long long>& ready) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  if (dyn_smem_bytes > 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  ready.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
 }
 
 // Programmatic dependent launch controls (no-ops without the launch attribute).

@@ -57,12 +57,23 @@ struct Seg {
   int32_t b, h;      // sequence, kv head
   int32_t lp0;       // first logical block of the run
   int32_t npages;    // pages in the run
-  int32_t k0;        // index of the run's first page within the slice
+  int32_t k0;        // index of the run's first page among the slice's pages
   int32_t len;       // sequence length (tokens)
   int32_t slot;      // partial slot (cta + unit), or -1 when written directly
   int32_t flags;     // kContPrev: continues the previous window's last run;
                      // kContNext: continues in the next window (no write yet)
+  long long us;      // the unit's first position on the cost line
 };
+
+// Cost-balanced partition. The (sequence, kv head, block) work list is laid
+// on a line where each non-empty unit occupies its pages followed by
+// `unit_cost` phantom positions (the per-unit work: query load, state
+// deposit and merge, partial write, expressed in pages); thread blocks take
+// equal slices of that line and process the real pages in theirs. Blocks
+// whose slice crosses many unit boundaries thus get fewer pages.
+__device__ __forceinline__ int unit_span(int pages, int unit_cost) {
+  return pages > 0 ? pages + unit_cost : 0;
+}
 
 template <int KV, int D, int BS>
 struct PageGeom {
@@ -108,7 +119,7 @@ struct DecodeParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* out;
-  int32_t* pre_pages;
+  int32_t* pre_cost;             // [batch + 1] per-head cost-line prefix of the sequences
   float* part_o;
   float* part_lse;
   unsigned long long* tickets;  // per unit: (epoch << 24) | slices finished
@@ -120,6 +131,7 @@ struct DecodeParams {
   int num_q_heads;
   int group;
   int max_blocks;
+  int unit_cost;                // phantom positions per unit on the cost line
   float scale_log2;
 };
 
@@ -1300,6 +1312,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   // block table, so the read-only planning below (lengths, slice, segment
   // list, block-table entries) overlaps it.
   pdl_launch_dependents();
+  // the TMA descriptor is fetched while the plan runs
+  if (tid == 0 && p.maps.valid) prefetch_tensormap(&p.maps.rec);
   bool waited = false;
   if (!p.early_plan) {
     pdl_wait();
@@ -1341,13 +1355,14 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     for (int b = tid; b < p.batch; b += kThreads) {
       const int len = seq_len_checked(p, b, cta == 0);
       if (b < kLensSmem) lens_sm[b] = len;
-      part += (len + BS - 1) / BS;
+      part += unit_span((len + BS - 1) / BS, p.unit_cost);
     }
     int tot;
     my_incl = block_incl_scan(part, warp_tot, tot);
     my_pages = part;
     npages_all = tot;
   }
+  // T: length of the cost line; this thread block's slice is [s_i, e_i)
   const long long T = npages_all * Hkv;
   const long long s_i = T * cta / Gc, e_i = T * (cta + 1) / Gc;
   // every thread block finds the sequence holding its first page
@@ -1361,7 +1376,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     int running = 0;
     for (int base = 0; base < p.batch; base += kThreads) {
       const int b = base + tid;
-      const int n = b < p.batch ? ((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS : 0;
+      const int n = b < p.batch ? unit_span(((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS, p.unit_cost) : 0;
       int tot;
       const int incl = block_incl_scan(n, warp_tot, tot);
       const long long lo = (long long)(running + incl - n) * Hkv;
@@ -1379,7 +1394,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       }
     }
   }
-  // CTA 0 publishes the per-sequence page prefix for the combine kernel (and,
+  // CTA 0 publishes the per-sequence cost prefix for the combine kernel (and,
   // with the in-kernel merge, zero rows for empty sequences): global writes,
   // so after the wait. lens_sm is still intact (no merge has run yet).
   bool published = false;
@@ -1392,21 +1407,21 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     }
     if (cta != 0) return;
     if (one_pass) {
-      if (tid < p.batch) p.pre_pages[tid] = my_incl - my_pages;
-      if (tid == p.batch - 1) p.pre_pages[p.batch] = my_incl;
+      if (tid < p.batch) p.pre_cost[tid] = my_incl - my_pages;
+      if (tid == p.batch - 1) p.pre_cost[p.batch] = my_incl;
     } else {
       int running = 0;
       for (int base = 0; base < p.batch; base += kThreads) {
         const int b = base + tid;
-        const int n = b < p.batch ? ((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS : 0;
+        const int n = b < p.batch ? unit_span(((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS, p.unit_cost) : 0;
         int tot;
         const int incl = block_incl_scan(n, warp_tot, tot);
-        if (b < p.batch) p.pre_pages[b] = running + incl - n;
-        if (b == p.batch - 1) p.pre_pages[p.batch] = running + incl;
+        if (b < p.batch) p.pre_cost[b] = running + incl - n;
+        if (b == p.batch - 1) p.pre_cost[p.batch] = running + incl;
         running += tot;
       }
     }
-    if (p.batch == 0 && tid == 0) p.pre_pages[0] = 0;
+    if (p.batch == 0 && tid == 0) p.pre_cost[0] = 0;
     if (p.fused) {
       // rows of empty sequences: no slice holds a page of them
       const int row_elems = p.num_q_heads * D;
@@ -1425,8 +1440,9 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     return;
   }
 
-  long long cur_b = plan[0], cur_base = plan[1];  // sequence holding `pos` and its first page
-  long long pos = s_i;
+  long long cur_b = plan[0], cur_base = plan[1];  // sequence holding `pos` and its start on the line
+  long long pos = s_i;       // cost-line position of the window
+  int k_done = 0;            // real pages of the slice in earlier windows
   int seg_counter = 0;      // segments started so far (q slot ring index)
   bool lens_cached = true;  // lens_sm valid until the first merge overwrites the stash
   uint64_t pol = policy_evict_first();
@@ -1437,6 +1453,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     // ---- build this window's segment list (warp 0)
     if (warp == 0) {
       int nseg = 0;
+      int kcount = k_done;  // real pages of the slice before the next segment
       long long b0 = cur_b, base0 = cur_base, wpos = pos;
       const long long wlim = min(e_i, pos + (long long)kMaxWinPages);
       bool done = false;
@@ -1445,16 +1462,17 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         const int len = bb >= p.batch ? 0
                         : (lens_cached && bb < kLensSmem) ? lens_sm[bb]
                                                           : seq_len_checked(p, (int)bb, false);
-        const int n = (len + BS - 1) / BS;
-        int x = n;
+        const int n = (len + BS - 1) / BS;  // real pages per unit
+        const int cn = unit_span(n, p.unit_cost);  // its span on the cost line
+        int x = cn;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, x, o);
           if (lane >= o) x += y;
         }
-        const long long my_base = base0 + (long long)(x - n) * Hkv;
-        const long long my_end = my_base + (long long)n * Hkv;
-        const bool overl = n > 0 && my_end > wpos && my_base < wlim && bb < p.batch;
+        const long long my_base = base0 + (long long)(x - cn) * Hkv;
+        const long long my_end = my_base + (long long)cn * Hkv;
+        const bool overl = cn > 0 && my_end > wpos && my_base < wlim && bb < p.batch;
         unsigned mask = __ballot_sync(0xffffffffu, overl);
         while (mask) {
           const int src = __ffs(mask) - 1;
@@ -1462,37 +1480,44 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           const long long sb = b0 + src;
           const long long sbase = __shfl_sync(0xffffffffu, my_base, src);
           const int sn = __shfl_sync(0xffffffffu, n, src);
+          const int scn = __shfl_sync(0xffffffffu, cn, src);
           const int slen = __shfl_sync(0xffffffffu, len, src);
-          const int h_lo = (int)max(0LL, (wpos - sbase) / sn);
-          const int h_hi = (int)min((long long)Hkv - 1, (wlim - 1 - sbase) / sn);
+          const int h_lo = (int)max(0LL, (wpos - sbase) / scn);
+          const int h_hi = (int)min((long long)Hkv - 1, (wlim - 1 - sbase) / scn);
           for (int h = h_lo; h <= h_hi && !done; ++h) {
-            const long long us = sbase + (long long)h * sn, ue = us + sn;
-            const long long lo = max(us, wpos), hi = min(ue, wlim);
-            if (lo >= hi) continue;
-            if (lane == 0) {
-              Seg sg;
-              sg.b = (int)sb;
-              sg.h = h;
-              sg.lp0 = (int)(lo - us);
-              sg.npages = (int)(hi - lo);
-              sg.k0 = (int)(lo - s_i);
-              sg.len = slen;
-              const long long first = owner_of(us, T, Gc), last = owner_of(ue - 1, T, Gc);
-              sg.slot = first == last ? -1 : (int)(cta + sb * Hkv + h);
-              // a unit's pages are contiguous within a slice: a run that starts
-              // after both the unit's and the slice's first page continues the
-              // previous window; one that stops before both ends goes on
-              sg.flags = (lo > us && lo > s_i ? kContPrev : 0) | (hi < ue && hi < e_i ? kContNext : 0);
-              segs[nseg] = sg;
+            // unit h: real pages [us, ure), then phantom positions up to ue
+            const long long us = sbase + (long long)h * scn, ure = us + sn, ue = us + scn;
+            const long long lo = max(us, wpos), hic = min(ue, wlim);
+            if (lo >= hic) continue;
+            const long long hi = min(ure, wlim);
+            if (lo < hi) {
+              if (lane == 0) {
+                Seg sg;
+                sg.b = (int)sb;
+                sg.h = h;
+                sg.lp0 = (int)(lo - us);
+                sg.npages = (int)(hi - lo);
+                sg.k0 = kcount;
+                sg.len = slen;
+                sg.us = us;
+                const long long first = owner_of(us, T, Gc), last = owner_of(ure - 1, T, Gc);
+                sg.slot = first == last ? -1 : (int)(cta + sb * Hkv + h);
+                // a unit's pages are contiguous within a slice: a run that starts
+                // after both the unit's and the slice's first page continues the
+                // previous window; one that stops before both ends goes on
+                sg.flags = (lo > us && lo > s_i ? kContPrev : 0) | (hi < ure && hi < e_i ? kContNext : 0);
+                segs[nseg] = sg;
+              }
+              ++nseg;
+              kcount += (int)(hi - lo);
             }
-            ++nseg;
-            wpos = hi;
-            if (hi >= wlim || nseg == kMaxSegs) {
+            wpos = hic;
+            if (hic >= wlim || nseg == kMaxSegs) {
               done = true;
               // the next window resumes at the sequence holding wpos
-              if (wpos >= sbase + (long long)sn * Hkv) {
+              if (wpos >= sbase + (long long)scn * Hkv) {
                 cur_b = sb + 1;
-                cur_base = sbase + (long long)sn * Hkv;
+                cur_base = sbase + (long long)scn * Hkv;
               } else {
                 cur_b = sb;
                 cur_base = sbase;
@@ -1511,6 +1536,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         plan[3] = wpos;
         plan[4] = cur_b;
         plan[5] = cur_base;
+        plan[6] = kcount;
       }
     }
     __syncthreads();
@@ -1518,7 +1544,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     const long long wend = plan[3];
     cur_b = plan[4];
     cur_base = plan[5];
-    const int kw0 = (int)(pos - s_i), kw1 = (int)(wend - s_i);
+    // the window's real pages are kw0 .. kw1 - 1 of the slice
+    const int kw0 = k_done, kw1 = (int)plan[6];
 
     {
       // the window's block-table entries -> shared memory, by every thread,
@@ -1744,7 +1771,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           __syncwarp();
           UnitSlices usl;
           usl.n = (sg.len + BS - 1) / BS;
-          usl.us = s_i + sg.k0 - sg.lp0;
+          usl.us = sg.us;
           usl.T = T;
           usl.G = Gc;
           usl.first = owner_of(usl.us, T, Gc);
@@ -1778,6 +1805,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     seg_counter += nseg;
     lens_cached = false;
     pos = wend;
+    k_done = kw1;
     __syncthreads();
   }
   // every issued copy was waited on by a consumer (or the abort path skipped
@@ -1805,26 +1833,30 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
 // one head and issues its loads for all slices back to back.
 template <int D>
 __global__ void __launch_bounds__(256)
-    splitkv_combine_kernel(const int32_t* seq_lens, const int32_t* pre_pages, const float* part_o,
+    splitkv_combine_kernel(const int32_t* seq_lens, const int32_t* pre_cost, const float* part_o,
                            const float* part_lse, float* out, int batch, int num_kv_heads, int group,
-                           int num_q_heads, int num_ctas, int block_size, int max_blocks, int lens_early) {
+                           int num_q_heads, int num_ctas, int block_size, int max_blocks, int unit_cost,
+                           int lens_early) {
   constexpr int kMaxSl = 64;  // slices handled from the precomputed mask; more go round again
   __shared__ long long sh_sum[2][8];
   pdl_launch_dependents();
   const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = u / num_kv_heads, j = u % num_kv_heads;
-  long long pre = 0, n = 0, T = 0;
+  // pre: the sequence's start on the cost line (per head); n: its pages; cn:
+  // its span per head; T: the line's length (the decode kernel's partition)
+  long long pre = 0, n = 0, cn = 0, T = 0;
   auto unit_range = [&](bool from_lens) {
     if (from_lens) {
-      // pages of every sequence and of those before b, from the lengths
+      // spans of every sequence and of those before b, from the lengths
       // (invalid lengths count as empty, as in the decode kernel)
       long long all = 0, before = 0;
       for (int x = tid; x < batch; x += blockDim.x) {
         const int len = seq_lens[x];
-        const long long np =
+        const int np =
             (len < 0 || (long long)len > (long long)max_blocks * block_size) ? 0 : (len + block_size - 1) / block_size;
-        all += np;
-        if (x < b) before += np;
+        const int span = unit_span(np, unit_cost);
+        all += span;
+        if (x < b) before += span;
         if (x == b) n = np;
       }
 #pragma unroll
@@ -1847,18 +1879,20 @@ __global__ void __launch_bounds__(256)
       if (b % (int)blockDim.x == tid) sh_sum[0][0] = n;
       __syncthreads();
       n = sh_sum[0][0];
+      cn = unit_span((int)n, unit_cost);
       pre = before;
       T = all * num_kv_heads;
     } else {
-      pre = pre_pages[b];
-      n = pre_pages[b + 1] - pre;
-      T = (long long)pre_pages[batch] * num_kv_heads;
+      pre = pre_cost[b];
+      cn = pre_cost[b + 1] - pre;
+      n = cn > 0 ? cn - unit_cost : 0;
+      T = (long long)pre_cost[batch] * num_kv_heads;
     }
   };
   UnitSlices usl;
   unsigned long long mask0 = 0;  // first round's slices that hold a partial
   auto unit_slices = [&]() {
-    usl.us = pre * num_kv_heads + (long long)j * n;
+    usl.us = pre * num_kv_heads + (long long)j * cn;
     usl.n = n;
     usl.T = T;
     usl.G = num_ctas;
@@ -1935,12 +1969,11 @@ template <int KV, int D, int BS, int G, int NS, bool TC>
 cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t stream) {
   using SM = Smem<KV, D, BS, G, NS, consumer_warps<KV, TC, BS>(), TC>;
   auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC>;
-  static bool attr_set = false;  // per instantiation; set before first launch
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::kBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> ready_dec{0}, ready_comb{0};  // per instantiation, per device
+  cudaError_t e = prepare_kernel(kern, (int)SM::kBytes, ready_dec);
+  if (e != cudaSuccess) return e;
+  e = prepare_kernel(splitkv_combine_kernel<D>, 0, ready_comb);
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1951,17 +1984,17 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+  e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return e;
   const int units = prm.batch * prm.pool.num_kv_heads;
   if (units == 0 || prm.fused) return cudaSuccess;
   cfg.gridDim = dim3(units);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D>, prm.seq_lens, (const int32_t*)prm.pre_pages,
+  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D>, prm.seq_lens, (const int32_t*)prm.pre_cost,
                             (const float*)prm.part_o, (const float*)prm.part_lse, prm.out, prm.batch,
                             prm.pool.num_kv_heads, prm.group, prm.num_q_heads, L.num_ctas, prm.pool.block_size,
-                            prm.max_blocks, prm.early_plan);
+                            prm.max_blocks, prm.unit_cost, prm.early_plan);
 }
 
 // Stages per consumer warp: as many pages in flight as the shared memory
@@ -2094,7 +2127,7 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& map
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
   ws += align256(sizeof(unsigned long long) * (size_t)L.batch * pool.num_kv_heads);
-  L.pre_pages = reinterpret_cast<int32_t*>(ws);
+  L.pre_cost = reinterpret_cast<int32_t*>(ws);
   ws += align256(sizeof(int32_t) * ((size_t)L.batch + 1));
   L.part_lse = reinterpret_cast<float*>(ws);
   ws += align256(sizeof(float) * slots * L.group);
@@ -2106,7 +2139,8 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& map
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
   prm.out = out;
-  prm.pre_pages = L.pre_pages;
+  prm.pre_cost = L.pre_cost;
+  prm.unit_cost = L.unit_cost;
   prm.part_o = L.part_o;
   prm.part_lse = L.part_lse;
   prm.tickets = tickets;

@@ -23,8 +23,9 @@ struct DecodeLaunch {
   bool fused_combine;   // merge split units inside the decode kernel
   bool early_plan;      // plan before waiting on the preceding kernel
   unsigned long long epoch;  // per-call tag of the merge tickets (40 bits, never 0)
+  int unit_cost;        // phantom pages per (sequence, kv head) unit in the partition
   // workspace carve-up
-  int32_t* pre_pages;   // [batch + 1] prefix sums of per-sequence block counts
+  int32_t* pre_cost;    // [batch + 1] per-head cost-line prefix of the sequences
   float* part_o;        // [num_ctas + batch*Hkv][group][D]
   float* part_lse;      // [num_ctas + batch*Hkv][group]
 };

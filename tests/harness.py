@@ -87,9 +87,10 @@ def assert_pools_equal(gpool, opool):
 
 
 def gpu_decode(gpool, wl, num_splits=0, out_fill=float("nan"), path="auto", combine="separate",
-               early_plan=False):
+               early_plan=False, unit_cost=-1):
     torch = torch_mod()
     gpool.set_decode_path(path, fused_combine=(combine == "fused"), early_plan=early_plan)
+    gpool.set_unit_cost(unit_cost)
     out = torch.full((wl.batch, wl.num_q_heads, wl.head_dim), out_fill, dtype=torch.float32,
                      device="cuda")
     gpool.decode(dev(wl.q_bits), dev(wl.block_table), dev(wl.seq_lens), wl.softmax_scale, out=out,

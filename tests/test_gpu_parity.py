@@ -56,6 +56,31 @@ def test_random_small(seed, dt):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("block_size", [16, 32])
+def test_unit_cost_partition(block_size, dt):
+    """The cost-balanced partition moves pages between thread blocks but never
+    changes the result: phantom pages per unit from none to far more than a
+    unit's pages (slices that hold only phantom positions, units cut into
+    many slices), empty and one-token sequences, with the separate and the
+    in-kernel merge."""
+    seq = [0, 1, 17, 200, 33, 0, 512, 3, 90]
+    wl = W.make_case(f"unit_cost_bs{block_size}", 93, len(seq), 8, 2, 128, block_size, dt, seq, extra_blocks=2,
+                     channel_offset_sigma=0.5 if dt != "bf16" else None)
+    g, o = H.load_both(wl)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    for path in _paths(dt, wl.head_dim):
+        for unit_cost in (0, 1, 5, 40, 4096):
+            for splits, combine, early in ((0, "separate", True), (7, "fused", False), (300, "separate", False)):
+                got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine, early_plan=early,
+                                   unit_cost=unit_cost)
+                H.check_attention(got, ref, f"{wl.name} {dt} unit_cost={unit_cost} splits={splits} {path} {combine}")
+    assert g.device_error() == (0, 0)
+    with pytest.raises(Exception):
+        g.set_unit_cost(5000)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
 def test_multi_step_tail_requant(dt):
     """Several decode steps, each appending one token per sequence into a
     partly filled block (re-quantised), then attending."""
