@@ -157,65 +157,72 @@ struct UnitSlices {
 };
 
 // Merge the partials of unit u into out rows row0 .. row0+group-1, by threads
-// tid = 0..nthr-1 (all of them call; `sync` synchronises exactly them).
-// wgt: shared scratch of 32 x 8 + 8 floats. Partials are read through L2
-// (written by other thread blocks of this launch).
-template <int D, typename Sync>
-__device__ __forceinline__ void merge_unit_partials(const UnitSlices& us, long long u, long long row0,
-                                                    int group, const float* part_o,
-                                                    const float* part_lse, float* out, int tid,
-                                                    int nthr, float* wgt, Sync sync) {
-  constexpr int kMaxSl = 32;
-  float* inv_tot = wgt + kMaxSl * 8;
-  const long long nsl = us.last - us.first + 1;
-  if (nsl <= kMaxSl) {
-    for (int i = tid; i < nsl * group; i += nthr) {
-      const int sl = i / group, h = i % group;
-      wgt[sl * 8 + h] = us.has_part(us.first + sl) ? __ldcg(part_lse + (us.first + sl + u) * group + h)
-                                                   : -INFINITY;
+// tid = 0..nthr-1: a thread owns four channels of one head per column and
+// up to kCols columns at a time, and folds the slices' (o, lse) pairs into a
+// running (M, W, A) online; every load of a round (kCols columns x kBatch
+// slices) is in flight at once. Partials are read through L2 (written by
+// other thread blocks of this launch). Not inlined: the decode loop keeps
+// its registers.
+template <int D>
+__device__ __noinline__ void merge_unit_partials(const UnitSlices& us, long long u, long long row0,
+                                                 int group, const float* __restrict__ part_o,
+                                                 const float* __restrict__ part_lse,
+                                                 float* __restrict__ out, int tid, int nthr) {
+  constexpr int kBatch = 4, kCols = 1;
+  const int ncol = group * D / 4;
+  for (int c0 = tid; c0 < ncol; c0 += nthr * kCols) {
+    float M[kCols], W[kCols], A[kCols][4];
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      M[j] = -INFINITY;
+      W[j] = 0.0f;
+      A[j][0] = A[j][1] = A[j][2] = A[j][3] = 0.0f;
     }
-    sync();
-    if (tid < group) {
-      float M = -INFINITY;
-      for (int sl = 0; sl < nsl; ++sl) M = fmaxf(M, wgt[sl * 8 + tid]);
-      float W = 0.0f;
-      for (int sl = 0; sl < nsl; ++sl) {
-        const float w = wgt[sl * 8 + tid] == -INFINITY ? 0.0f : exp2f(wgt[sl * 8 + tid] - M);
-        wgt[sl * 8 + tid] = w;
-        W += w;
+    for (long long i0 = us.first; i0 <= us.last; i0 += kBatch) {
+      bool has[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) has[k] = i0 + k <= us.last && us.has_part(i0 + k);
+      float l[kCols][kBatch];
+      float4 o[kCols][kBatch];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        const int col = c0 + j * nthr;
+        const int e0 = col * 4, h = e0 / D;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          l[j][k] = -INFINITY;
+          o[j][k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (col < ncol && has[k]) {
+            const long long slot = i0 + k + u;
+            l[j][k] = __ldcg(part_lse + slot * group + h);
+            o[j][k] = __ldcg(reinterpret_cast<const float4*>(part_o + slot * group * D + e0));
+          }
+        }
       }
-      inv_tot[tid] = W > 0.0f ? 1.0f / W : 0.0f;
+#pragma unroll
+      for (int j = 0; j < kCols; ++j)
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (l[j][k] == -INFINITY) continue;
+          const float Mn = fmaxf(M[j], l[j][k]);
+          const float a = M[j] == -INFINITY ? 0.0f : exp2f(M[j] - Mn), w = exp2f(l[j][k] - Mn);
+          W[j] = W[j] * a + w;
+          A[j][0] = A[j][0] * a + w * o[j][k].x;
+          A[j][1] = A[j][1] * a + w * o[j][k].y;
+          A[j][2] = A[j][2] * a + w * o[j][k].z;
+          A[j][3] = A[j][3] * a + w * o[j][k].w;
+          M[j] = Mn;
+        }
     }
-    sync();
-    for (int e = tid; e < group * D; e += nthr) {
-      const int h = e / D;
-      float A = 0.0f;
-#pragma unroll 4
-      for (int sl = 0; sl < nsl; ++sl) {
-        const float w = wgt[sl * 8 + h];
-        if (w != 0.0f) A += w * __ldcg(part_o + (us.first + sl + u) * group * D + e);
-      }
-      out[row0 * D + e] = A * inv_tot[h];
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      const int col = c0 + j * nthr;
+      if (col >= ncol) continue;
+      const float inv = W[j] > 0.0f ? 1.0f / W[j] : 0.0f;
+      *reinterpret_cast<float4*>(out + row0 * D + col * 4) =
+          make_float4(A[j][0] * inv, A[j][1] * inv, A[j][2] * inv, A[j][3] * inv);
     }
-    sync();
-    return;
   }
-  for (int e = tid; e < group * D; e += nthr) {
-    const int h = e / D;
-    float M = -INFINITY;
-    for (long long i = us.first; i <= us.last; ++i)
-      if (us.has_part(i)) M = fmaxf(M, __ldcg(part_lse + (i + u) * group + h));
-    float W = 0.0f, A = 0.0f;
-    for (long long i = us.first; i <= us.last; ++i) {
-      if (!us.has_part(i)) continue;
-      const float l = __ldcg(part_lse + (i + u) * group + h);
-      const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
-      W += w;
-      A += w * __ldcg(part_o + (i + u) * group * D + e);
-    }
-    out[row0 * D + e] = W > 0.0f ? A / W : 0.0f;
-  }
-  sync();
 }
 
 // Sequence length clamped to what the table can hold; bad lengths count as 0.
@@ -1763,10 +1770,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         else
           merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.part_o + (long long)sg.slot * g * D,
                                                                   p.part_lse + (long long)sg.slot * g);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merged);  // the stash may be overwritten
         if (sg.slot >= 0 && p.fused) {
           // the last slice to finish this unit merges its partials (threadfence
-          // reduction: partials are fenced before the ticket is taken); the
-          // stash, read out above, is the scratch
+          // reduction: partials are fenced before the ticket is taken)
           __threadfence();
           __syncwarp();
           UnitSlices usl;
@@ -1794,12 +1802,9 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           last_slice = __shfl_sync(0xffffffffu, last_slice, 0);
           if (last_slice) {
             __threadfence();
-            merge_unit_partials<D>(usl, u, row0, g, p.part_o, p.part_lse, p.out, lane, 32, stash_acc,
-                                   [] { __syncwarp(); });
+            merge_unit_partials<D>(usl, u, row0, g, p.part_o, p.part_lse, p.out, lane, 32);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(merged);  // the stash may be overwritten
       }
     }
     seg_counter += nseg;
