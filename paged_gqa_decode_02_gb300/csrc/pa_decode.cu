@@ -1372,6 +1372,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   // T: length of the cost line; this thread block's slice is [s_i, e_i)
   const long long T = npages_all * Hkv;
   const long long s_i = T * cta / Gc, e_i = T * (cta + 1) / Gc;
+  // Ring stages in use (of the NST allocated): about one per 8 pages of a
+  // slice, 16 to 24. Short slices run better with fewer pages in flight (the
+  // first copies land sooner and HBM queues stay short); long ones need the
+  // depth. The same for every thread block of the launch.
+  const int nst = (int)max((long long)min(NST, kConsumerWarps), min((long long)NST, max(16LL, min(24LL, T / Gc / 8))));
   // every thread block finds the sequence holding its first page
   if (one_pass) {
     const long long lo = (long long)(my_incl - my_pages) * Hkv, hi = (long long)my_incl * Hkv;
@@ -1555,9 +1560,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     const int kw0 = k_done, kw1 = (int)plan[6];
 
     {
-      // the window's block-table entries -> shared memory, by every thread,
-      // kStageLoads independent loads in flight per thread (one round trip
-      // for windows of up to kStageLoads * kThreads pages)
+      // the window's page records -> shared memory: the block-table entry
+      // of each page, checked and turned into its record index (block * Hkv
+      // + head; -1 for an entry outside the pool), by every thread with
+      // kStageLoads independent loads in flight (one round trip for windows
+      // of up to kStageLoads * kThreads pages)
       constexpr int kStageLoads = 4;
       const int nwin = kw1 - kw0;
       for (int i0 = 0; i0 < nwin; i0 += kStageLoads * kThreads) {
@@ -1574,7 +1581,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
               if (segs[mid].k0 <= k) lo = mid; else hi = mid - 1;
             }
             const Seg& sg = segs[lo];
-            v[u] = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
+            const int phys = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
+            v[u] = (phys < 0 || phys >= p.pool.num_blocks) ? -1 : phys * Hkv + sg.h;
           }
         }
 #pragma unroll
@@ -1590,7 +1598,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- producer
       // (2) issue in sub-batches, lane j taking page k + j. A sub-batch holds
-      // at most one page per stage (<= NST pages): the previous fill of each
+      // at most one page per stage (<= nst pages): the previous fill of each
       // lane's stage was issued by an earlier sub-batch, after the release of
       // the fill before it, so each parity wait below sees its barrier at most
       // one phase behind. (Two lanes on one stage could see a barrier two
@@ -1642,28 +1650,27 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         // the next segment's q goes out as soon as its slot is free, a ring's
         // worth of pages before the consumers need it
         if (lane == 0 && q_sent == qseg && q_sent < nseg && send_q(q_sent, false)) ++q_sent;
-        int kend = min(kw1, k + (NST < 32 ? NST : 32));
+        int kend = min(kw1, k + (nst < 32 ? nst : 32));
         if (qseg < nseg) kend = min(kend, segs[qseg].k0);
         const int kk = k + lane;
         if (kk < kend) {
-          const Seg& sg = segs[qseg - 1];  // the sub-batch lies inside this segment
-          const int phys = phys_s[kk - kw0];
-          const int stage = kk % NST;
-          const int n = kk / NST;
+          const int rec = phys_s[kk - kw0];  // record index, -1 for a bad table entry
+          const int stage = kk % nst;
+          const int n = kk / nst;
           bool ok = true;
           if (n >= 1 && !abort_flag) ok = mbar_wait_bounded(&empty[stage], (n - 1) & 1);
           if (!ok) {
             set_error(p.pool.err, PA_DEVERR_TIMEOUT);
             abort_flag = 1;
           }
-          if (phys < 0 || phys >= p.pool.num_blocks || abort_flag) {
+          if (rec < 0 || abort_flag) {
             if (!abort_flag) set_error(p.pool.err, PA_DEVERR_BLOCK_TABLE);
             stage_flag[stage] = 1;
             mbar_arrive(&full[stage]);
           } else {
             stage_flag[stage] = 0;
             uint8_t* dst = stages + (size_t)stage * PG::kStageBytes;
-            const long long page = (long long)phys * Hkv + sg.h;
+            const long long page = rec;
             issued_n[stage] = n;
             mbar_arrive_expect_tx(&full[stage], PG::kStageBytes);
             if (TC && KV != PA_KV_BF16) {
@@ -1712,9 +1719,9 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         if (lane == 0) mbar_arrive(&qempty[slot]);
         // my pages: k = k0 + i with k % W == cw
         const int kfirst = sg.k0 + ((cw - sg.k0 % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+        // ring position of k, advanced without dividing (kConsumerWarps <= nst)
+        int stage = kfirst % nst, n = kfirst / nst;
         for (int k = kfirst; k < sg.k0 + sg.npages; k += kConsumerWarps) {
-          const int stage = k % NST;
-          const int n = k / NST;
           bool okp = abort_flag == 0 && mbar_wait_bounded(&full[stage], n & 1);
           if (!okp && abort_flag == 0) {
             if (lane == 0) set_error(p.pool.err, PA_DEVERR_TIMEOUT);
@@ -1727,6 +1734,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
+          stage += kConsumerWarps;
+          if (stage >= nst) {
+            stage -= nst;
+            ++n;
+          }
         }
         if (sg.flags & kContNext) continue;  // the run goes on in the next window
         // ---- hand this warp's state of the unit to the merger warp and go on
