@@ -43,7 +43,8 @@ WORKLOAD_TEXT = {
 
 
 PROFILE_FOR = {"qwen25_7b_bf16": "profiles/paged_gqa_decode_qwen25_7b_bf16.md",
-               "qwen3_8b_int8": "profiles/paged_gqa_decode_qwen3_8b_int8.md"}
+               "qwen3_8b_int8": "profiles/paged_gqa_decode_qwen3_8b_int8.md",
+               "long_uint4": "profiles/paged_gqa_decode_long_uint4.md"}
 
 
 def _traffic(workload, path):
