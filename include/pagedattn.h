@@ -235,6 +235,60 @@ PA_API const char* pa_status_string(pa_status s);
 /* Message of the last failed call on this thread ("" if none). */
 PA_API const char* pa_last_error(void);
 
+/* ---- Host block manager (which physical blocks hold which sequence's tokens)
+ *
+ * Host-side bookkeeping for a pool's physical blocks (TFFInfer article,
+ * section 3.6.4 KVCache: PageManager; heterogeneous engine article, section
+ * 2.3 paged KV and its prefix sharing): a free list, each sequence's block
+ * table (token t in slot t % block_size of table[t / block_size]), reference
+ * counts for blocks that sequences share, and
+ *  - a prefix cache: a full block is known by the chained hash of the token
+ *    ids of all blocks up to it; a sequence admitted with a prompt whose
+ *    leading full blocks are cached shares those blocks, whose KV is already
+ *    written (with an unmatched prompt's full blocks entered into the cache
+ *    when admitted: the caller writes their KV before any later reader runs
+ *    on the same stream);
+ *  - fork: a child shares all of its parent's blocks;
+ *  - copy-on-write: before a sequence writes into a partly filled block that
+ *    another sequence also holds, the block is replaced by a private one and
+ *    a (src, dst) pair is returned for the caller to copy (pa_copy_blocks).
+ * Blocks no sequence holds that are cached stay cached and are reused least
+ * recently released first. Host memory only, no device work; not
+ * thread-safe (one manager per scheduling thread). Token ids may be NULL when
+ * the prefix cache is off. Calls that fail (PA_ERR_INVALID_ARG, or
+ * PA_ERR_OOM when the blocks run out) change nothing. */
+typedef struct pa_block_manager pa_block_manager;
+PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t block_size, int32_t prefix_cache,
+                              pa_block_manager** out);
+PA_API pa_status pa_bm_destroy(pa_block_manager* bm);
+/* Admit sequence `seq_id` holding `n_tokens` prompt tokens; *n_cached_tokens
+ * (optional) receives how many leading tokens are in shared cached blocks
+ * (a multiple of block_size), whose KV need not be written again. */
+PA_API pa_status pa_bm_add_sequence(pa_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                                    int32_t n_tokens, int32_t* n_cached_tokens);
+PA_API pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent_id, int64_t child_id);
+/* Reserve slots for `n_tokens` more tokens of a sequence (a decode step: 1).
+ * At most one copy is returned (the shared partly filled last block); the
+ * caller copies it before writing. Blocks this call fills join the cache. */
+PA_API pa_status pa_bm_append_tokens(pa_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                                     int32_t n_tokens, int32_t* copy_src, int32_t* copy_dst,
+                                     int32_t copy_capacity, int32_t* n_copies);
+PA_API pa_status pa_bm_free_sequence(pa_block_manager* bm, int64_t seq_id);
+/* The sequence's block table into table[0 .. max_blocks) (-1 padded), its
+ * block count and token count (each optional). PA_ERR_INVALID_ARG when the
+ * table does not fit (the counts are still written). */
+PA_API pa_status pa_bm_block_table(const pa_block_manager* bm, int64_t seq_id, int32_t* table,
+                                   int32_t max_blocks, int32_t* num_blocks, int64_t* seq_len);
+/* Blocks that can be handed out: free ones plus cached ones nobody holds. */
+PA_API int32_t pa_bm_num_free_blocks(const pa_block_manager* bm);
+/* Sequences holding `block` (-1 for a bad id). */
+PA_API int32_t pa_bm_ref_count(const pa_block_manager* bm, int32_t block);
+
+/* Device: copy whole blocks (the page records of every kv head) src[i] ->
+ * dst[i] in a pool, for copy-on-write. src, dst: host arrays of n block ids,
+ * src[i] != dst[i]. Enqueued on `stream`. */
+PA_API pa_status pa_copy_blocks(pa_pool* pool, const int32_t* src, const int32_t* dst, int32_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

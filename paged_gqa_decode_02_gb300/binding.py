@@ -14,6 +14,8 @@ import os
 import re
 import threading
 
+import numpy as np
+
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +79,27 @@ def lib():
         L.pa_pool_set_decode_path.restype = I32
         L.pa_pool_set_unit_cost.argtypes = [P, I32]
         L.pa_pool_set_unit_cost.restype = I32
+        I64, PI32 = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32)
+        L.pa_bm_create.argtypes = [I32, I32, I32, ctypes.POINTER(P)]
+        L.pa_bm_create.restype = I32
+        L.pa_bm_destroy.argtypes = [P]
+        L.pa_bm_destroy.restype = I32
+        L.pa_bm_add_sequence.argtypes = [P, I64, P, I32, PI32]
+        L.pa_bm_add_sequence.restype = I32
+        L.pa_bm_fork.argtypes = [P, I64, I64]
+        L.pa_bm_fork.restype = I32
+        L.pa_bm_append_tokens.argtypes = [P, I64, P, I32, PI32, PI32, I32, PI32]
+        L.pa_bm_append_tokens.restype = I32
+        L.pa_bm_free_sequence.argtypes = [P, I64]
+        L.pa_bm_free_sequence.restype = I32
+        L.pa_bm_block_table.argtypes = [P, I64, P, I32, PI32, ctypes.POINTER(I64)]
+        L.pa_bm_block_table.restype = I32
+        L.pa_bm_num_free_blocks.argtypes = [P]
+        L.pa_bm_num_free_blocks.restype = I32
+        L.pa_bm_ref_count.argtypes = [P, I32]
+        L.pa_bm_ref_count.restype = I32
+        L.pa_copy_blocks.argtypes = [P, P, P, I32, P]
+        L.pa_copy_blocks.restype = I32
         L.pa_decode_num_splits.argtypes = [P, I32]
         L.pa_decode_num_splits.restype = I32
         L.pa_pool_view.argtypes = [P, ctypes.POINTER(pa_pool_buffers)]
@@ -222,6 +245,15 @@ class PagedKVPool:
                 "v_scale": comp(b.v_scale, D * 4, torch.float32),
                 "v_zp": comp(b.v_zp, D * 4, torch.int32)}
 
+    def copy_blocks(self, src, dst, stream=None):
+        """Copy whole blocks src[i] -> dst[i] (copy-on-write of shared blocks)."""
+        s_ = np.ascontiguousarray(src, dtype=np.int32)
+        d_ = np.ascontiguousarray(dst, dtype=np.int32)
+        assert s_.size == d_.size
+        st = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        _check(lib().pa_copy_blocks(self.handle, s_.ctypes.data_as(ctypes.c_void_p), d_.ctypes.data_as(ctypes.c_void_p),
+                                    int(s_.size), ctypes.c_void_p(st)))
+
     def append_kv(self, k_new, v_new, cu_new, ctx_lens, block_table, max_new_per_seq=0, stream=None):
         B = int(ctx_lens.shape[0])
         pa_append_kv(self.handle, k_new, v_new, cu_new, ctx_lens, block_table, B,
@@ -268,3 +300,81 @@ class PagedKVPool:
 
     def device_error(self, stream=None):
         return pa_get_device_error(self.handle, stream)
+
+
+class BlockManager:
+    """Host block manager of a pool's physical blocks (see pa_bm_create): free
+    list, per-sequence block tables, shared blocks with reference counts, a
+    prefix cache of full blocks keyed by their token-id chain, fork and
+    copy-on-write. Host memory only."""
+
+    def __init__(self, num_blocks, block_size, prefix_cache=True):
+        h = ctypes.c_void_p()
+        _check(lib().pa_bm_create(int(num_blocks), int(block_size), 1 if prefix_cache else 0, ctypes.byref(h)))
+        self.handle = h
+        self.block_size = int(block_size)
+
+    @staticmethod
+    def _tokens(tokens):
+        if tokens is None:
+            return None, 0
+        a = np.ascontiguousarray(tokens, dtype=np.int32)
+        return a, int(a.size)
+
+    def add_sequence(self, seq_id, tokens=None, n_tokens=None):
+        """Admit a sequence; returns how many leading tokens sit in cached blocks."""
+        a, n = self._tokens(tokens)
+        if a is None:
+            n = int(n_tokens)
+        cached = ctypes.c_int32(0)
+        _check(lib().pa_bm_add_sequence(self.handle, int(seq_id), None if a is None else a.ctypes.data_as(ctypes.c_void_p),
+                                        n, ctypes.byref(cached)))
+        return int(cached.value)
+
+    def fork(self, parent_id, child_id):
+        _check(lib().pa_bm_fork(self.handle, int(parent_id), int(child_id)))
+
+    def append_tokens(self, seq_id, tokens=None, n_tokens=None):
+        """Reserve slots for more tokens; returns the (src, dst) block copies the
+        caller must do before writing (copy-on-write), at most one."""
+        a, n = self._tokens(tokens)
+        if a is None:
+            n = int(n_tokens)
+        src, dst, nc = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(0)
+        _check(lib().pa_bm_append_tokens(self.handle, int(seq_id), None if a is None else a.ctypes.data_as(ctypes.c_void_p),
+                                         n, ctypes.byref(src), ctypes.byref(dst), 1, ctypes.byref(nc)))
+        return [(int(src.value), int(dst.value))] if nc.value else []
+
+    def free_sequence(self, seq_id):
+        _check(lib().pa_bm_free_sequence(self.handle, int(seq_id)))
+
+    def block_table(self, seq_id, max_blocks=None):
+        """(block ids as an int32 array of length max_blocks (-1 padded) or of
+        the sequence's block count, token count)."""
+        nb, ln = ctypes.c_int32(0), ctypes.c_int64(0)
+        if max_blocks is None:  # ask for the count first (a zero-size table)
+            st = lib().pa_bm_block_table(self.handle, int(seq_id), None, 0, ctypes.byref(nb), ctypes.byref(ln))
+            if st != 0 and nb.value == 0:
+                _check(st)
+        m = nb.value if max_blocks is None else int(max_blocks)
+        t = np.full(max(m, 1), -1, dtype=np.int32)
+        _check(lib().pa_bm_block_table(self.handle, int(seq_id), t.ctypes.data_as(ctypes.c_void_p), m,
+                                       ctypes.byref(nb), ctypes.byref(ln)))
+        return t[:m], int(ln.value)
+
+    def num_free_blocks(self):
+        return int(lib().pa_bm_num_free_blocks(self.handle))
+
+    def ref_count(self, block):
+        return int(lib().pa_bm_ref_count(self.handle, int(block)))
+
+    def close(self):
+        if self.handle:
+            lib().pa_bm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

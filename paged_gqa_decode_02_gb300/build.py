@@ -23,6 +23,7 @@ SOURCES = {
     "pa_api.cu": [],
     "pa_append.cu": ["--fmad=false"],
     "pa_decode.cu": [],
+    "pa_block_manager.cpp": [],
 }
 
 
@@ -40,7 +41,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     objs, procs = [], []
     for src, flags in SOURCES.items():
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _newer(o, [s] + headers):
             cmd = [NVCC] + ARCH + COMMON + list(flags) + list(extra_flags) + ["-c", s, "-o", o]

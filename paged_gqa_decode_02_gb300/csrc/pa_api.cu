@@ -214,6 +214,26 @@ pa_status pa_pool_view(const pa_pool* p, pa_pool_buffers* out) {
   return PA_OK;
 }
 
+pa_status pa_copy_blocks(pa_pool* p, const int32_t* src, const int32_t* dst, int32_t n, void* stream) {
+  g_last_error[0] = 0;
+  if (!p || n < 0 || (n > 0 && (!src || !dst))) return fail(PA_ERR_INVALID_ARG, "null pool or block lists, or n < 0%s");
+  for (int32_t i = 0; i < n; ++i)
+    if (src[i] < 0 || src[i] >= p->desc.num_blocks || dst[i] < 0 || dst[i] >= p->desc.num_blocks || src[i] == dst[i])
+      return fail(PA_ERR_INVALID_ARG, "block id out of range, or a block copied onto itself%s");
+  if (n == 0) return PA_OK;
+  DeviceGuard dg(p->desc.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  // a block's records (one per kv head) are contiguous: one copy per block
+  const size_t bytes = (size_t)p->desc.num_kv_heads * (size_t)p->dev.stride;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < n; ++i) {
+    const cudaError_t e = cudaMemcpyAsync(p->dev.k + (size_t)dst[i] * bytes, p->dev.k + (size_t)src[i] * bytes, bytes,
+                                          cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "block copy");
+  }
+  return PA_OK;
+}
+
 pa_status pa_get_device_error(pa_pool* p, void* stream, uint32_t* flags) {
   g_last_error[0] = 0;
   if (!p || !flags) return fail(PA_ERR_INVALID_ARG, "null pool or flags%s");
