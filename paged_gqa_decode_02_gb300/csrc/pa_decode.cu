@@ -717,15 +717,25 @@ struct MmaConsumerU8 {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, q = lane & 3;
     const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
-    const uint32_t kb = sb + PG::kOffK;
-    const uint32_t vb = sb + PG::kOffV;
+    // Swizzled addresses in closed form: the stage base is 1024-aligned and
+    // each array starts on a known row phase (static_asserts below), so every
+    // load is a per-lane base XOR a constant plus an immediate (checked
+    // against the generic swizzle for all lanes).
+    static_assert(PG::kOffK == 0 && PG::kOffV % 1024 == 0, "code rows start on an 8-row boundary");
+    static_assert((PG::kOffKs / 128) % 8 == 0 && (PG::kOffKz / 128) % 8 == 4 &&
+                      (PG::kOffVs / 128) % 8 == 0 && (PG::kOffVz / 128) % 8 == 4,
+                  "metadata row phases");
+    const uint32_t bq = sb + 16 * q;                 // K scales / zero points
+    const uint32_t bg = sb + 16 * gq;                // V scales / zero points
+    const uint32_t bk = sb + 144 * gq + 4 * q;       // K codes, row gq
+    const uint32_t bv = sb + PG::kOffV + 288 * q + 16 * (gq >> 2) + 4 * (gq & 3);  // V codes, row 2q
 
     // ---- w = q * scale of head gq and its largest magnitude
     float w[32];
     float amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      const float4 sc = lds_f4(sw(sb, PG::kOffKs + 64 * k + 16 * q));
+      const float4 sc = lds_f4((bq ^ (16 * (k >> 1))) + PG::kOffKs + 128 * (k >> 1) + 64 * (k & 1));
       w[4 * k + 0] = bf16_lo(qp[2 * k]) * sc.x;
       w[4 * k + 1] = bf16_hi(qp[2 * k]) * sc.y;
       w[4 * k + 2] = bf16_lo(qp[2 * k + 1]) * sc.z;
@@ -753,7 +763,7 @@ struct MmaConsumerU8 {
     float bias = 0.0f;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      const int4 z = lds_i4(sw(sb, PG::kOffKz + 64 * k + 16 * q));
+      const int4 z = lds_i4((bq ^ (16 * (k >> 1))) + PG::kOffKz + 128 * (k >> 1) + 64 * ((k & 1) ^ 1));
       const float w0 = w[4 * k] * f, w1 = w[4 * k + 1] * f, w2 = w[4 * k + 2] * f, w3 = w[4 * k + 3] * f;
       bias = fmaf(w0, (float)z.x, bias);
       bias = fmaf(w1, (float)z.y, bias);
@@ -764,10 +774,10 @@ struct MmaConsumerU8 {
       const uint32_t bl0 = pack_f16(w0 - h01.x, w1 - h01.y), bl1 = pack_f16(w2 - h23.x, w3 - h23.y);
 #pragma unroll
       for (int tt = 0; tt < TT; ++tt) {
-        const int r0 = tt * 16 + gq, r1 = r0 + 8;
+        const uint32_t ka = (bk ^ (16 * k)) + tt * 16 * ROW;  // rows tt*16 + gq and + 8
         uint32_t c0, c1;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(kb + r0 * ROW + ((k ^ (r0 & 7)) << 4) + 4 * q) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(kb + r1 * ROW + ((k ^ (r1 & 7)) << 4) + 4 * q) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(ka) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(ka + 8 * ROW) : "memory");
         uint32_t a[4];
         a[0] = bytes_to_f16x2(c0, 0x4140);
         a[1] = bytes_to_f16x2(c1, 0x4140);
@@ -839,15 +849,14 @@ struct MmaConsumerU8 {
 #pragma unroll
     for (int pr = 0; pr < 4; ++pr) {
       float raw0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, raw1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const int chunk = 2 * pr + (gq >> 2), cofs = 4 * (gq & 3);
+      const uint32_t va = bv ^ (32 * pr), vo = va ^ 16;  // rows 2q (+8) and 2q + 1 (+8)
 #pragma unroll
       for (int tt = 0; tt < TT; ++tt) {
-        const int t0 = tt * 16 + 2 * q, t1 = t0 + 1, t2 = t0 + 8, t3 = t0 + 9;
-        uint32_t W0, W1, W2, W3;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W0) : "r"(vb + t0 * ROW + ((chunk ^ (t0 & 7)) << 4) + cofs) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W1) : "r"(vb + t1 * ROW + ((chunk ^ (t1 & 7)) << 4) + cofs) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W2) : "r"(vb + t2 * ROW + ((chunk ^ (t2 & 7)) << 4) + cofs) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W3) : "r"(vb + t3 * ROW + ((chunk ^ (t3 & 7)) << 4) + cofs) : "memory");
+        uint32_t W0, W1, W2, W3;  // tokens tt*16 + 2q + {0, 1, 8, 9}
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W0) : "r"(va + tt * 16 * ROW) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W1) : "r"(vo + tt * 16 * ROW + ROW) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W2) : "r"(va + tt * 16 * ROW + 8 * ROW) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W3) : "r"(vo + tt * 16 * ROW + 9 * ROW) : "memory");
         const uint32_t u01 = prmt(W0, W1, 0x5140), u23 = prmt(W0, W1, 0x7362);
         const uint32_t v01 = prmt(W2, W3, 0x5140), v23 = prmt(W2, W3, 0x7362);
         uint32_t A0[4], A1[4];
@@ -866,8 +875,8 @@ struct MmaConsumerU8 {
       }
       // fold: o = alpha o + scale (raw - zp * sum_p)
       const int c0 = 32 * pr + 4 * gq;
-      const float4 sc = lds_f4(sw(sb, PG::kOffVs + 4 * c0));
-      const int4 z = lds_i4(sw(sb, PG::kOffVz + 4 * c0));
+      const float4 sc = lds_f4((bg ^ (16 * pr)) + PG::kOffVs + 128 * pr);   // channels c0 .. c0 + 3
+      const int4 z = lds_i4((bg ^ (16 * (4 ^ pr))) + PG::kOffVz + 128 * pr);
       float* oa = o[2 * pr];
       float* ob = o[2 * pr + 1];
       oa[0] = fmaf(a0, oa[0], sc.x * fmaf(-(float)z.x, sum0, raw0[0]));
