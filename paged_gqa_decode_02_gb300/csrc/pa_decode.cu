@@ -1353,10 +1353,10 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     fence_mbar_init();
   }
 
-  // ---- plan: total pages, this slice, and where it starts. Checked lengths
-  // of the first kLensSmem sequences are kept in shared memory (in the merge
-  // stash, idle until the first merge) for the second pass and the first
-  // window's segment list.
+  // ---- plan: the cost line, this slice, and where it starts. Checked
+  // lengths of the first kLensSmem sequences are kept in shared memory (in
+  // the merge stash, idle until the consumer warps start) for a second pass
+  // and the first window's segment list.
   int* lens_sm = reinterpret_cast<int*>(stash_acc);
   constexpr int kLensSmem = (int)(SM::kStashAccBytes / 4);
   // With at most one sequence per thread (the usual case) one block scan
@@ -1417,7 +1417,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   }
   // CTA 0 publishes the per-sequence cost prefix for the combine kernel (and,
   // with the in-kernel merge, zero rows for empty sequences): global writes,
-  // so after the wait. lens_sm is still intact (no merge has run yet).
+  // so after the wait. lens_sm is still intact (the consumers have not
+  // started).
   bool published = false;
   auto wait_and_publish = [&]() {
     if (published) return;
@@ -1465,7 +1466,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   long long pos = s_i;       // cost-line position of the window
   int k_done = 0;            // real pages of the slice in earlier windows
   int seg_counter = 0;      // segments started so far (q slot ring index)
-  bool lens_cached = true;  // lens_sm valid until the first merge overwrites the stash
+  bool lens_cached = true;  // lens_sm valid until the consumer warps write the stash
   uint64_t pol = policy_evict_first();
   Cons cons;  // consumer warps' online-softmax state; persists across windows
   int n_dep = 0;  // units this warp has deposited (phase of `merged` to wait for)
