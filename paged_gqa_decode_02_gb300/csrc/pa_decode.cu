@@ -1000,14 +1000,26 @@ struct MmaConsumerU4 {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, q = lane & 3;
     const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
+    // Swizzled addresses in closed form (a per-lane base XOR a constant plus
+    // an immediate; the stage base is 1024-aligned and each array starts on
+    // a known row phase), checked against the generic swizzle for all lanes.
+    static_assert(PG::kOffK == 0 && PG::kOffV % 1024 == 0, "code rows start on an 8-row boundary");
+    static_assert((PG::kOffKs / 128) % 8 == 0 && (PG::kOffKz / 128) % 8 == 4 &&
+                      (PG::kOffVs / 128) % 8 == 0 && (PG::kOffVz / 128) % 8 == 4,
+                  "metadata row phases");
+    const uint32_t bq = sb + 32 * q;  // K scales / zero points
+    const uint32_t bkc = sb + 128 * (gq >> 1) + 64 * (gq & 1) + 16 * (gq >> 1) + 4 * q;  // K codes, row gq
+    const uint32_t bvc = sb + PG::kOffV + 128 * q + 16 * ((gq >> 2) ^ q) + 4 * (gq & 3);  // V codes, row 2q
+    const uint32_t bvm = sb + 128 * (gq >> 2) + 32 * (gq & 3) + 16 * (gq >> 2);  // V scales / zero points
 
     // ---- w = q * scale of head gq (channels 32k + 8q + j) and its largest magnitude
     float w[32];
     float amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float4 s0 = lds_f4(sw(sb, PG::kOffKs + 4 * (32 * k + 8 * q)));
-      const float4 s1 = lds_f4(sw(sb, PG::kOffKs + 4 * (32 * k + 8 * q) + 16));
+      const uint32_t ks = (bq ^ (32 * (k >> 1))) + PG::kOffKs + 128 * k;
+      const float4 s0 = lds_f4(ks + 16 * (k & 1));
+      const float4 s1 = lds_f4(ks + 16 * ((k & 1) ^ 1));
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -1033,8 +1045,9 @@ struct MmaConsumerU4 {
     float bias = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int4 z0 = lds_i4(sw(sb, PG::kOffKz + 4 * (32 * k + 8 * q)));
-      const int4 z1 = lds_i4(sw(sb, PG::kOffKz + 4 * (32 * k + 8 * q) + 16));
+      const uint32_t kz = (bq ^ (32 * (k >> 1)) ^ 64) + PG::kOffKz + 128 * k;
+      const int4 z0 = lds_i4(kz + 16 * (k & 1));
+      const int4 z1 = lds_i4(kz + 16 * ((k & 1) ^ 1));
       const int zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
       float ws[8];
 #pragma unroll
@@ -1055,9 +1068,9 @@ struct MmaConsumerU4 {
       }
 #pragma unroll
       for (int tt = 0; tt < TT; ++tt) {
-        const int r0 = tt * 16 + gq, r1 = r0 + 8;
-        const uint32_t c0 = lds_u32(sw(sb, PG::kOffK + r0 * ROWB + 16 * k + 4 * q));
-        const uint32_t c1 = lds_u32(sw(sb, PG::kOffK + r1 * ROWB + 16 * k + 4 * q));
+        const uint32_t ka = (bkc ^ (16 * k)) + tt * 16 * ROWB;  // rows tt*16 + gq and + 8
+        const uint32_t c0 = lds_u32(ka);
+        const uint32_t c1 = lds_u32((ka ^ 64) + 8 * ROWB);
         const uint32_t lo0 = c0 & 0x0F0F0F0Fu, hi0 = (c0 >> 4) & 0x0F0F0F0Fu;
         const uint32_t lo1 = c1 & 0x0F0F0F0Fu, hi1 = (c1 >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
@@ -1135,12 +1148,11 @@ struct MmaConsumerU4 {
         for (int i = 0; i < 4; ++i) raw[sd][i] = 0.0f;
 #pragma unroll
       for (int tt = 0; tt < TT; ++tt) {
-        const int t0 = tt * 16 + 2 * q;
-        const uint32_t cb = PG::kOffV + 32 * oc + 4 * gq;
-        const uint32_t W0 = lds_u32(sw(sb, cb + t0 * ROWB));
-        const uint32_t W1 = lds_u32(sw(sb, cb + (t0 + 1) * ROWB));
-        const uint32_t W2 = lds_u32(sw(sb, cb + (t0 + 8) * ROWB));
-        const uint32_t W3 = lds_u32(sw(sb, cb + (t0 + 9) * ROWB));
+        const uint32_t va = (bvc ^ (32 * oc)) + tt * 16 * ROWB;  // tokens tt*16 + 2q + {0, 1, 8, 9}
+        const uint32_t W0 = lds_u32(va);
+        const uint32_t W1 = lds_u32(va ^ 64);
+        const uint32_t W2 = lds_u32((va ^ 64) + 8 * ROWB);
+        const uint32_t W3 = lds_u32(va + 8 * ROWB);
         const uint32_t l0w = W0 & 0x0F0F0F0Fu, l1w = W1 & 0x0F0F0F0Fu, l2w = W2 & 0x0F0F0F0Fu, l3w = W3 & 0x0F0F0F0Fu;
         const uint32_t h0w = (W0 >> 4) & 0x0F0F0F0Fu, h1w = (W1 >> 4) & 0x0F0F0F0Fu;
         const uint32_t h2w = (W2 >> 4) & 0x0F0F0F0Fu, h3w = (W3 >> 4) & 0x0F0F0F0Fu;
@@ -1160,9 +1172,10 @@ struct MmaConsumerU4 {
           mma_f16_16816(raw[sd], A, pl[tt][0], pl[tt][1]);
         }
       }
-      const int c0 = 64 * oc + 8 * gq;
-      const float4 s0 = lds_f4(sw(sb, PG::kOffVs + 4 * c0)), s1 = lds_f4(sw(sb, PG::kOffVs + 4 * c0 + 16));
-      const int4 z0 = lds_i4(sw(sb, PG::kOffVz + 4 * c0)), z1 = lds_i4(sw(sb, PG::kOffVz + 4 * c0 + 16));
+      const uint32_t vs = (bvm ^ (32 * oc)) + PG::kOffVs + 256 * oc;  // channels 64oc + 8gq .. + 7
+      const uint32_t vz = (bvm ^ (32 * oc) ^ 64) + PG::kOffVz + 256 * oc;
+      const float4 s0 = lds_f4(vs), s1 = lds_f4(vs ^ 16);
+      const int4 z0 = lds_i4(vz), z1 = lds_i4(vz ^ 16);
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
       const float zf[8] = {(float)z0.x, (float)z0.y, (float)z0.z, (float)z0.w,
                            (float)z1.x, (float)z1.y, (float)z1.z, (float)z1.w};
