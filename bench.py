@@ -47,19 +47,39 @@ PROFILE_FOR = {"qwen25_7b_bf16": "profiles/paged_gqa_decode_qwen25_7b_bf16.md",
                "long_uint4": "profiles/paged_gqa_decode_long_uint4.md"}
 
 
+# The consumer sections of the decode source each workload's tensor-core
+# kernel compiles from; the other consumers' sections do not reach its code.
+_CONSUMER_SECTIONS = ("consumer math (CUDA cores)", "consumer math (tensor cores)",
+                      "consumer math (tensor cores, uint8 KV)", "consumer math (tensor cores, uint4 KV)")
+_USES = {"qwen25_7b_bf16": "consumer math (tensor cores)", "prefix_mix": "consumer math (tensor cores)",
+         "qwen3_8b_int8": "consumer math (tensor cores, uint8 KV)",
+         "long_uint4": "consumer math (tensor cores, uint4 KV)"}
+
+
+def kernel_source_hash(workload):
+    """sha256 (16 hex digits) of the decode source this workload's tensor-core
+    kernel is compiled from: the decode and common sources without the
+    sections of the consumers it does not use."""
+    import hashlib
+    src = open(os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_decode.cu")).read()
+    keep = _USES[workload]
+    parts = src.split("// " + "-" * 66 + " ")
+    kept = [parts[0]] + [x for x in parts[1:] if not (x.split("\n", 1)[0].strip() in _CONSUMER_SECTIONS
+                                                       and x.split("\n", 1)[0].strip() != keep)]
+    common = open(os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_common.cuh")).read()
+    return hashlib.sha256(("".join(kept) + common).encode()).hexdigest()[:16]
+
+
 def _traffic(workload, path):
     """DRAM bytes per decode launch from the committed ncu summary, or None
-    when there is none for this workload or the kernel source changed since."""
-    import hashlib
+    when there is none for this workload or the kernel's source changed since."""
     rel = PROFILE_FOR.get(workload)
     if rel is None or path not in ("auto", "tensor_core"):
         return None
     try:
         text = open(os.path.join(ROOT, rel)).read()
-        fields = dict(l.split(": ", 1) for l in text.splitlines() if l.startswith(("traffic_", "source_")))
-        src = b"".join(open(os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc", f), "rb").read()
-                       for f in ("pa_decode.cu", "pa_common.cuh"))
-        if hashlib.sha256(src).hexdigest()[:16] != fields["source_sha256_16"].strip():
+        fields = dict(l.split(": ", 1) for l in text.splitlines() if l.startswith(("traffic_", "kernel_source_")))
+        if kernel_source_hash(workload) != fields["kernel_source_sha256_16"].strip():
             return None
         return int(fields["traffic_bytes_per_launch"])
     except Exception:
