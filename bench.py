@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -56,18 +57,31 @@ _USES = {"qwen25_7b_bf16": "consumer math (tensor cores)", "prefix_mix": "consum
          "long_uint4": "consumer math (tensor cores, uint4 KV)"}
 
 
-def kernel_source_hash(workload):
-    """sha256 (16 hex digits) of the decode source this workload's tensor-core
+_C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(text):
+    """C/CUDA source with its comments removed, trailing blanks stripped and
+    empty lines dropped: two sources that differ only in comments or blank
+    lines compile to the same kernel and give the same text."""
+    text = _C_TOKENS.sub(lambda m: " " if m.group(0)[0] == "/" else m.group(0), text)
+    return "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+
+
+def kernel_source_hash(workload, decode_src=None, common_src=None):
+    """sha256 (16 hex digits) of the code this workload's tensor-core decode
     kernel is compiled from: the decode and common sources without the
-    sections of the consumers it does not use."""
+    sections of the consumers it does not use, comments and blank lines
+    removed. The sources default to the files in the tree."""
     import hashlib
-    src = open(os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_decode.cu")).read()
+    csrc = os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc")
+    src = decode_src if decode_src is not None else open(os.path.join(csrc, "pa_decode.cu")).read()
+    common = common_src if common_src is not None else open(os.path.join(csrc, "pa_common.cuh")).read()
     keep = _USES[workload]
     parts = src.split("// " + "-" * 66 + " ")
     kept = [parts[0]] + [x for x in parts[1:] if not (x.split("\n", 1)[0].strip() in _CONSUMER_SECTIONS
                                                        and x.split("\n", 1)[0].strip() != keep)]
-    common = open(os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_common.cuh")).read()
-    return hashlib.sha256(("".join(kept) + common).encode()).hexdigest()[:16]
+    return hashlib.sha256((_code_only("".join(kept)) + "\n" + _code_only(common)).encode()).hexdigest()[:16]
 
 
 def _traffic(workload, path):

@@ -10,21 +10,22 @@
 //
 // Work decomposition (a GB300 design; the pages' sketch used one warp per
 // head): a "unit" is one (sequence, kv head) pair and serves all g query
-// heads of its group. The units' blocks are concatenated in (b, j, block)
-// order into one list of T pages; thread block i of G takes the contiguous
-// slice [i*T/G, (i+1)*T/G). Every SM therefore streams the same number of
-// bytes whatever the length mix. A unit that lies inside one slice is
-// written straight to `out`; a unit cut by slice boundaries leaves one
-// partial (o = acc / l, lse = m + log2 l) per slice, merged by the combine
-// kernel with log-sum-exp weights.
+// heads of its group. The units are laid in (b, j) order on a cost line,
+// each non-empty unit taking its pages plus a fixed number of phantom
+// positions for its per-unit work; thread block i of G takes the slice
+// [i*C/G, (i+1)*C/G) of that line and processes the real pages in it, so
+// every SM gets the same share of work whatever the length mix. A unit that
+// lies inside one slice is written straight to `out`; a unit cut by slice
+// boundaries leaves one partial (o = acc / l, lse = m + log2 l) per slice,
+// merged by the combine kernel with log-sum-exp weights.
 //
-// Inside a thread block: warp 0 is the producer. It reads block-table entries
-// 32 at a time and issues 1-D TMA bulk copies (cp.async.bulk) of each page's
-// K and V (plus scales / zero points) into a ring of shared-memory stages,
-// one sub-ring per consumer warp, completing on mbarriers. Consumer warps
-// take pages round-robin, keep a private online-softmax state per unit
-// (fp32, max/sum reductions with warp shuffles), and merge their states
-// through shared memory at the end of each unit.
+// Inside a thread block: warp 0 is the producer. It sends each run's query
+// rows by a bulk copy and issues the pages (K and V, plus the scales and
+// zero points of quantised pools) into a ring of shared-memory stages by
+// TMA, completing on mbarriers. Consumer warps take pages round-robin and
+// keep a private online-softmax state per unit (fp32); at the end of a
+// unit's run each deposits its state in a shared-memory stash, and a merger
+// warp merges the deposited states and writes the row or the partial.
 //
 // Every wait is bounded: on expiry the thread block records
 // PA_DEVERR_TIMEOUT, stops waiting and computing, keeps the barrier sequence
