@@ -30,6 +30,8 @@ from typing import List, Optional
 import numpy as np
 
 KV_DTYPES = ("bf16", "uint8", "uint4")
+# every storage format a case may name; random cases draw from KV_DTYPES
+ALL_KV_DTYPES = KV_DTYPES + ("fp8",)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -181,7 +183,7 @@ def make_case(name, seed, batch, num_q_heads, num_kv_heads, head_dim, block_size
               seq_lens, extra_blocks=0, channel_offset_sigma=None, max_blocks=None,
               softmax_scale=None) -> Workload:
     """Generic seeded case with private (unshared) blocks."""
-    assert kv_dtype in KV_DTYPES
+    assert kv_dtype in ALL_KV_DTYPES
     seq_lens = np.asarray(seq_lens, np.int32)
     assert seq_lens.shape == (batch,)
     nbs = [-(-int(s) // block_size) for s in seq_lens]
