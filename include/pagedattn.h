@@ -284,10 +284,55 @@ PA_API int32_t pa_bm_num_free_blocks(const pa_block_manager* bm);
 /* Sequences holding `block` (-1 for a bad id). */
 PA_API int32_t pa_bm_ref_count(const pa_block_manager* bm, int32_t block);
 
+/* CPU swap tier (engine article, section 4.3: the block manager's swap_out
+ * moves GPU blocks to a CPU second-level cache, swap_in brings them back).
+ * The caller owns a host buffer of num_cpu_blocks slots of
+ * pa_pool_block_bytes each and applies each returned copy list with
+ * pa_swap_blocks, in call order on one stream.
+ *  - pa_bm_set_cpu_blocks: size the host tier (slots 0 .. n-1); refused
+ *    while any slot is in use.
+ *  - pa_bm_swap_out: every block of a resident sequence is copied to a slot
+ *    of its own (gpu_src[i] -> cpu_dst[i], i < *n_copies) and released on
+ *    the GPU (blocks other sequences hold stay; an idle cached block stays
+ *    cached). The sequence is then swapped out: append, fork and block table
+ *    are refused for it until pa_bm_swap_in.
+ *  - pa_bm_swap_in: fresh GPU blocks for each slot (cpu_src[i] ->
+ *    gpu_dst[i]); the slots are freed.
+ *  - pa_bm_swapped_slots: a swapped-out sequence's slots, in token order.
+ * Capacities are in entries; PA_ERR_OOM when slots or blocks run out, and
+ * failed calls change nothing. Freeing a swapped-out sequence frees its
+ * slots. */
+PA_API pa_status pa_bm_set_cpu_blocks(pa_block_manager* bm, int32_t num_cpu_blocks);
+PA_API int32_t pa_bm_num_free_cpu_blocks(const pa_block_manager* bm);
+PA_API pa_status pa_bm_swap_out(pa_block_manager* bm, int64_t seq_id, int32_t* gpu_src, int32_t* cpu_dst,
+                                int32_t capacity, int32_t* n_copies);
+PA_API pa_status pa_bm_swap_in(pa_block_manager* bm, int64_t seq_id, int32_t* cpu_src, int32_t* gpu_dst,
+                               int32_t capacity, int32_t* n_copies);
+PA_API pa_status pa_bm_swapped_slots(const pa_block_manager* bm, int64_t seq_id, int32_t* slots,
+                                     int32_t capacity, int32_t* n_slots);
+
 /* Device: copy whole blocks (the page records of every kv head) src[i] ->
  * dst[i] in a pool, for copy-on-write. src, dst: host arrays of n block ids,
  * src[i] != dst[i]. Enqueued on `stream`. */
 PA_API pa_status pa_copy_blocks(pa_pool* pool, const int32_t* src, const int32_t* dst, int32_t n, void* stream);
+
+/* Bytes of one block's page records (all kv heads): the size of a host slot
+ * of the swap tier. 0 for a NULL pool. */
+PA_API size_t pa_pool_block_bytes(const pa_pool* pool);
+
+/* Device <-> host: copy whole blocks between the pool and a caller-owned host
+ * buffer of num_host_blocks slots of pa_pool_block_bytes each (pinned memory
+ * for asynchronous copies). direction PA_SWAP_OUT copies block blocks[i] to
+ * slot slots[i], PA_SWAP_IN slot slots[i] to block blocks[i]. blocks, slots:
+ * host arrays of n ids. One cudaMemcpyAsync per block, enqueued on `stream`;
+ * the caller keeps the buffer alive until they complete.
+ * Errors: PA_ERR_INVALID_ARG (null pool or buffer, ids out of range, unknown
+ * direction; nothing enqueued), PA_ERR_CUDA. */
+#define PA_SWAP_OUT 0
+#define PA_SWAP_IN 1
+PA_API pa_status pa_swap_blocks(pa_pool* pool, void* host_buffer, int32_t num_host_blocks,
+                                const int32_t* blocks, const int32_t* slots, int32_t n, int32_t direction,
+                                void* stream);
 
 #ifdef __cplusplus
 }

@@ -27,6 +27,7 @@ KV_DTYPES = {"bf16": PA_KV_BF16, "uint8": PA_KV_UINT8, "uint4": PA_KV_UINT4}
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
           4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE_BOUNDS", 6: "PA_ERR_TIMEOUT"}
 DEVERR_BLOCK_TABLE, DEVERR_SEQ_LEN, DEVERR_APPEND, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 
 
 class PagedAttnError(RuntimeError):
@@ -100,6 +101,20 @@ def lib():
         L.pa_bm_ref_count.restype = I32
         L.pa_copy_blocks.argtypes = [P, P, P, I32, P]
         L.pa_copy_blocks.restype = I32
+        L.pa_pool_block_bytes.argtypes = [P]
+        L.pa_pool_block_bytes.restype = ctypes.c_size_t
+        L.pa_swap_blocks.argtypes = [P, P, I32, P, P, I32, I32, P]
+        L.pa_swap_blocks.restype = I32
+        L.pa_bm_set_cpu_blocks.argtypes = [P, I32]
+        L.pa_bm_set_cpu_blocks.restype = I32
+        L.pa_bm_num_free_cpu_blocks.argtypes = [P]
+        L.pa_bm_num_free_cpu_blocks.restype = I32
+        L.pa_bm_swap_out.argtypes = [P, I64, P, P, I32, PI32]
+        L.pa_bm_swap_out.restype = I32
+        L.pa_bm_swap_in.argtypes = [P, I64, P, P, I32, PI32]
+        L.pa_bm_swap_in.restype = I32
+        L.pa_bm_swapped_slots.argtypes = [P, I64, P, I32, PI32]
+        L.pa_bm_swapped_slots.restype = I32
         L.pa_decode_num_splits.argtypes = [P, I32]
         L.pa_decode_num_splits.restype = I32
         L.pa_pool_view.argtypes = [P, ctypes.POINTER(pa_pool_buffers)]
@@ -254,6 +269,25 @@ class PagedKVPool:
         _check(lib().pa_copy_blocks(self.handle, s_.ctypes.data_as(ctypes.c_void_p), d_.ctypes.data_as(ctypes.c_void_p),
                                     int(s_.size), ctypes.c_void_p(st)))
 
+    def block_bytes(self):
+        """Bytes of one block's page records (a slot of the host swap tier)."""
+        return int(lib().pa_pool_block_bytes(self.handle))
+
+    def swap_blocks(self, host_buffer, blocks, slots, direction, stream=None):
+        """Copy whole blocks between the pool and `host_buffer` (a uint8 CPU
+        tensor of whole slots, pinned for asynchronous copies): direction
+        "out" copies blocks[i] -> slot slots[i], "in" slot slots[i] -> blocks[i]."""
+        b_ = np.ascontiguousarray(blocks, dtype=np.int32)
+        s_ = np.ascontiguousarray(slots, dtype=np.int32)
+        assert b_.size == s_.size and host_buffer.dtype == torch.uint8 and not host_buffer.is_cuda
+        assert host_buffer.is_contiguous()
+        d = {"out": PA_SWAP_OUT, "in": PA_SWAP_IN}[direction]
+        st = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        _check(lib().pa_swap_blocks(self.handle, ctypes.c_void_p(host_buffer.data_ptr()),
+                                    int(host_buffer.numel() // self.block_bytes()),
+                                    b_.ctypes.data_as(ctypes.c_void_p), s_.ctypes.data_as(ctypes.c_void_p),
+                                    int(b_.size), d, ctypes.c_void_p(st)))
+
     def append_kv(self, k_new, v_new, cu_new, ctx_lens, block_table, max_new_per_seq=0, stream=None):
         B = int(ctx_lens.shape[0])
         pa_append_kv(self.handle, k_new, v_new, cu_new, ctx_lens, block_table, B,
@@ -364,6 +398,42 @@ class BlockManager:
 
     def num_free_blocks(self):
         return int(lib().pa_bm_num_free_blocks(self.handle))
+
+    # ---- CPU swap tier
+    def set_cpu_blocks(self, num_cpu_blocks):
+        _check(lib().pa_bm_set_cpu_blocks(self.handle, int(num_cpu_blocks)))
+
+    def num_free_cpu_blocks(self):
+        return int(lib().pa_bm_num_free_cpu_blocks(self.handle))
+
+    def swap_out(self, seq_id):
+        """Move a resident sequence to host slots; returns the (gpu block,
+        host slot) copies to make (PagedKVPool.swap_blocks, "out")."""
+        n = len(self.block_table(seq_id)[0])
+        src, dst, nc = np.zeros(max(n, 1), np.int32), np.zeros(max(n, 1), np.int32), ctypes.c_int32(0)
+        _check(lib().pa_bm_swap_out(self.handle, int(seq_id), src.ctypes.data_as(ctypes.c_void_p),
+                                    dst.ctypes.data_as(ctypes.c_void_p), n, ctypes.byref(nc)))
+        return [(int(a), int(b)) for a, b in zip(src[:nc.value], dst[:nc.value])]
+
+    def swap_in(self, seq_id):
+        """Bring a swapped-out sequence back into fresh GPU blocks; returns the
+        (host slot, gpu block) copies to make (PagedKVPool.swap_blocks, "in")."""
+        n = len(self.swapped_slots(seq_id))
+        src, dst, nc = np.zeros(max(n, 1), np.int32), np.zeros(max(n, 1), np.int32), ctypes.c_int32(0)
+        _check(lib().pa_bm_swap_in(self.handle, int(seq_id), src.ctypes.data_as(ctypes.c_void_p),
+                                   dst.ctypes.data_as(ctypes.c_void_p), n, ctypes.byref(nc)))
+        return [(int(a), int(b)) for a, b in zip(src[:nc.value], dst[:nc.value])]
+
+    def swapped_slots(self, seq_id):
+        """Host slots of a swapped-out sequence, in token order."""
+        n = ctypes.c_int32(0)
+        st = lib().pa_bm_swapped_slots(self.handle, int(seq_id), None, 0, ctypes.byref(n))
+        if st != 0 and n.value == 0:
+            _check(st)
+        a = np.zeros(max(n.value, 1), np.int32)
+        _check(lib().pa_bm_swapped_slots(self.handle, int(seq_id), a.ctypes.data_as(ctypes.c_void_p), n.value,
+                                         ctypes.byref(n)))
+        return [int(x) for x in a[:n.value]]
 
     def ref_count(self, block):
         return int(lib().pa_bm_ref_count(self.handle, int(block)))

@@ -234,6 +234,38 @@ pa_status pa_copy_blocks(pa_pool* p, const int32_t* src, const int32_t* dst, int
   return PA_OK;
 }
 
+size_t pa_pool_block_bytes(const pa_pool* p) {
+  return p ? (size_t)p->desc.num_kv_heads * (size_t)p->dev.stride : 0;
+}
+
+pa_status pa_swap_blocks(pa_pool* p, void* host_buffer, int32_t num_host_blocks, const int32_t* blocks,
+                         const int32_t* slots, int32_t n, int32_t direction, void* stream) {
+  g_last_error[0] = 0;
+  if (!p || !host_buffer || num_host_blocks < 0 || n < 0 || (n > 0 && (!blocks || !slots)))
+    return fail(PA_ERR_INVALID_ARG, "null pool, buffer or id lists, or a negative count%s");
+  if (direction != PA_SWAP_OUT && direction != PA_SWAP_IN)
+    return fail(PA_ERR_INVALID_ARG, "direction must be PA_SWAP_OUT or PA_SWAP_IN%s");
+  for (int32_t i = 0; i < n; ++i)
+    if (blocks[i] < 0 || blocks[i] >= p->desc.num_blocks || slots[i] < 0 || slots[i] >= num_host_blocks)
+      return fail(PA_ERR_INVALID_ARG, "block id or host slot out of range%s");
+  if (n == 0) return PA_OK;
+  DeviceGuard dg(p->desc.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  // a block's records (one per kv head) are contiguous: one copy per block
+  const size_t bytes = pa_pool_block_bytes(p);
+  uint8_t* host = static_cast<uint8_t*>(host_buffer);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < n; ++i) {
+    uint8_t* dev = p->dev.k + (size_t)blocks[i] * bytes;
+    uint8_t* hst = host + (size_t)slots[i] * bytes;
+    const cudaError_t e = direction == PA_SWAP_OUT
+                              ? cudaMemcpyAsync(hst, dev, bytes, cudaMemcpyDeviceToHost, s)
+                              : cudaMemcpyAsync(dev, hst, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "block swap copy");
+  }
+  return PA_OK;
+}
+
 pa_status pa_get_device_error(pa_pool* p, void* stream, uint32_t* flags) {
   g_last_error[0] = 0;
   if (!p || !flags) return fail(PA_ERR_INVALID_ARG, "null pool or flags%s");

@@ -17,6 +17,16 @@
 //    copies the page records: pa_copy_blocks).
 // Cached blocks that no sequence holds stay cached until their slot is
 // needed (least recently released first).
+//
+// CPU swap tier (the heterogeneous engine article, section 4.3: the block
+// manager's swap_out moves GPU blocks to a CPU second-level cache and
+// swap_in brings them back): a swapped-out
+// sequence holds host slots instead of GPU blocks. Swapping out copies every
+// block of the sequence to a slot of its own and releases the GPU blocks
+// (blocks other sequences still hold stay on the GPU; an idle cached block
+// stays in the prefix cache until reused); swapping in takes fresh GPU blocks
+// and frees the slots. The caller moves the page records with the returned
+// copy lists (pa_swap_blocks), in call order on one stream.
 #include <algorithm>
 #include <cstdint>
 #include <list>
@@ -38,7 +48,8 @@ struct Block {
 };
 
 struct Sequence {
-  std::vector<int32_t> blocks;
+  std::vector<int32_t> blocks;  // GPU blocks, or host slots while swapped out
+  bool swapped = false;
   int64_t len = 0;
   uint64_t tail_hash = 0;       // chain hash through the last full block (0: none)
   std::vector<int32_t> tail;    // token ids of the partly filled last block (prefix cache)
@@ -68,6 +79,8 @@ struct pa_block_manager {
   std::list<int32_t> idle_cached;                // cached, ref == 0, oldest first
   std::unordered_map<uint64_t, int32_t> cache;   // chain hash -> block
   std::unordered_map<int64_t, Sequence> seqs;
+  std::vector<int32_t> cpu_free;                 // free host slots
+  int32_t cpu_blocks = 0;
 
   int32_t available() const { return (int32_t)(free_list.size() + idle_cached.size()); }
 
@@ -193,7 +206,7 @@ pa_status pa_bm_add_sequence(pa_block_manager* bm, int64_t seq_id, const int32_t
 pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent_id, int64_t child_id) {
   if (!bm || bm->seqs.count(child_id)) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(parent_id);
-  if (it == bm->seqs.end()) return PA_ERR_INVALID_ARG;
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_INVALID_ARG;
   Sequence child = it->second;
   for (int32_t b : child.blocks) bm->hold(b);
   bm->seqs.emplace(child_id, std::move(child));
@@ -204,7 +217,7 @@ pa_status pa_bm_append_tokens(pa_block_manager* bm, int64_t seq_id, const int32_
                               int32_t* copy_src, int32_t* copy_dst, int32_t copy_capacity, int32_t* n_copies) {
   if (!bm || n_tokens < 0 || (n_tokens > 0 && bm->prefix_cache && !tokens)) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_INVALID_ARG;
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_INVALID_ARG;
   Sequence& sq = it->second;
   const int32_t bs = bm->block_size;
   if (n_copies) *n_copies = 0;
@@ -246,8 +259,12 @@ pa_status pa_bm_free_sequence(pa_block_manager* bm, int64_t seq_id) {
   if (!bm) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end()) return PA_ERR_INVALID_ARG;
-  // release tail first, so that a chain's leaf is evicted before its root
-  for (auto b = it->second.blocks.rbegin(); b != it->second.blocks.rend(); ++b) bm->release(*b);
+  if (it->second.swapped) {
+    for (int32_t c : it->second.blocks) bm->cpu_free.push_back(c);
+  } else {
+    // release tail first, so that a chain's leaf is evicted before its root
+    for (auto b = it->second.blocks.rbegin(); b != it->second.blocks.rend(); ++b) bm->release(*b);
+  }
   bm->seqs.erase(it);
   return PA_OK;
 }
@@ -256,7 +273,7 @@ pa_status pa_bm_block_table(const pa_block_manager* bm, int64_t seq_id, int32_t*
                             int32_t* num_blocks, int64_t* seq_len) {
   if (!bm || max_blocks < 0 || (max_blocks > 0 && !table)) return PA_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_INVALID_ARG;
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_INVALID_ARG;
   const Sequence& sq = it->second;
   if (num_blocks) *num_blocks = (int32_t)sq.blocks.size();
   if (seq_len) *seq_len = sq.len;
@@ -267,6 +284,75 @@ pa_status pa_bm_block_table(const pa_block_manager* bm, int64_t seq_id, int32_t*
 }
 
 int32_t pa_bm_num_free_blocks(const pa_block_manager* bm) { return bm ? bm->available() : 0; }
+
+pa_status pa_bm_set_cpu_blocks(pa_block_manager* bm, int32_t num_cpu_blocks) {
+  if (!bm || num_cpu_blocks < 0) return PA_ERR_INVALID_ARG;
+  if ((int32_t)bm->cpu_free.size() != bm->cpu_blocks) return PA_ERR_INVALID_ARG;  // slots in use
+  bm->cpu_blocks = num_cpu_blocks;
+  bm->cpu_free.clear();
+  for (int32_t c = num_cpu_blocks - 1; c >= 0; --c) bm->cpu_free.push_back(c);  // hand out 0, 1, 2, ...
+  return PA_OK;
+}
+
+int32_t pa_bm_num_free_cpu_blocks(const pa_block_manager* bm) { return bm ? (int32_t)bm->cpu_free.size() : 0; }
+
+pa_status pa_bm_swap_out(pa_block_manager* bm, int64_t seq_id, int32_t* gpu_src, int32_t* cpu_dst,
+                         int32_t capacity, int32_t* n_copies) {
+  if (!bm || !n_copies) return PA_ERR_INVALID_ARG;
+  *n_copies = 0;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_INVALID_ARG;
+  Sequence& sq = it->second;
+  const int32_t n = (int32_t)sq.blocks.size();
+  if (n > 0 && (!gpu_src || !cpu_dst || capacity < n)) return PA_ERR_INVALID_ARG;
+  if (n > (int32_t)bm->cpu_free.size()) return PA_ERR_OOM;
+  std::vector<int32_t> slots((size_t)n);
+  for (int32_t i = 0; i < n; ++i) {
+    slots[(size_t)i] = bm->cpu_free.back();
+    bm->cpu_free.pop_back();
+    gpu_src[i] = sq.blocks[(size_t)i];
+    cpu_dst[i] = slots[(size_t)i];
+  }
+  for (auto b = sq.blocks.rbegin(); b != sq.blocks.rend(); ++b) bm->release(*b);
+  sq.blocks = std::move(slots);
+  sq.swapped = true;
+  *n_copies = n;
+  return PA_OK;
+}
+
+pa_status pa_bm_swap_in(pa_block_manager* bm, int64_t seq_id, int32_t* cpu_src, int32_t* gpu_dst,
+                        int32_t capacity, int32_t* n_copies) {
+  if (!bm || !n_copies) return PA_ERR_INVALID_ARG;
+  *n_copies = 0;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end() || !it->second.swapped) return PA_ERR_INVALID_ARG;
+  Sequence& sq = it->second;
+  const int32_t n = (int32_t)sq.blocks.size();
+  if (n > 0 && (!cpu_src || !gpu_dst || capacity < n)) return PA_ERR_INVALID_ARG;
+  if (n > bm->available()) return PA_ERR_OOM;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t b = bm->take();
+    cpu_src[i] = sq.blocks[(size_t)i];
+    gpu_dst[i] = b;
+    bm->cpu_free.push_back(sq.blocks[(size_t)i]);
+    sq.blocks[(size_t)i] = b;
+  }
+  sq.swapped = false;
+  *n_copies = n;
+  return PA_OK;
+}
+
+pa_status pa_bm_swapped_slots(const pa_block_manager* bm, int64_t seq_id, int32_t* slots, int32_t capacity,
+                              int32_t* n_slots) {
+  if (!bm || !n_slots || capacity < 0 || (capacity > 0 && !slots)) return PA_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end() || !it->second.swapped) return PA_ERR_INVALID_ARG;
+  const std::vector<int32_t>& v = it->second.blocks;
+  *n_slots = (int32_t)v.size();
+  if ((int32_t)v.size() > capacity) return PA_ERR_INVALID_ARG;
+  std::copy(v.begin(), v.end(), slots);
+  return PA_OK;
+}
 
 int32_t pa_bm_ref_count(const pa_block_manager* bm, int32_t block) {
   if (!bm || block < 0 || block >= (int32_t)bm->blocks.size()) return -1;

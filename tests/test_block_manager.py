@@ -1,5 +1,6 @@
 """Host block manager (pa_bm_*): block tables, shared blocks, prefix cache,
-fork and copy-on-write. Host logic only; runs without a GPU.
+fork, copy-on-write and the CPU swap tier. Host logic only; runs without a
+GPU.
 
 The randomized test drives the manager the way a caller does. A simulated
 store keeps a token id per (block, slot); the caller applies the manager's
@@ -9,7 +10,9 @@ table. After every operation these must hold:
   - no block is written while another sequence also holds it;
   - a prefix-cache hit's blocks already hold the prompt's tokens;
   - reference counts equal the number of tables holding each block;
-  - free blocks plus held blocks add up to the pool."""
+  - free blocks plus held blocks add up to the pool;
+  - a swapped-out sequence reads back its tokens through its host slots,
+    each slot held by one sequence, and free plus held slots add up."""
 import numpy as np
 import pytest
 
@@ -118,14 +121,92 @@ def test_failed_calls_change_nothing():
     assert bm.ref_count(-1) == -1 and bm.ref_count(4) == -1
 
 
-class _Caller:
-    """A caller of the manager with a simulated KV store (token ids)."""
+def test_swap_out_and_in_round_trip():
+    bs = 4
+    bm = B.BlockManager(8, bs)
+    bm.set_cpu_blocks(5)
+    bm.add_sequence(1, list(range(10)))  # 3 blocks
+    t1, _ = bm.block_table(1)
+    copies = bm.swap_out(1)
+    assert copies == [(int(t1[0]), 0), (int(t1[1]), 1), (int(t1[2]), 2)]
+    assert bm.swapped_slots(1) == [0, 1, 2] and bm.num_free_cpu_blocks() == 2
+    assert bm.num_free_blocks() == 8
+    for call in (lambda: bm.block_table(1), lambda: bm.append_tokens(1, [5]), lambda: bm.fork(1, 2),
+                 lambda: bm.swap_out(1)):
+        with pytest.raises(B.PagedAttnError):
+            call()
+    bm.add_sequence(2, [9] * 30)  # takes all 8 blocks
+    with pytest.raises(B.PagedAttnError) as e:
+        bm.swap_in(1)  # no GPU blocks: refused, nothing changed
+    assert e.value.status == 3 and bm.swapped_slots(1) == [0, 1, 2]
+    bm.free_sequence(2)
+    back = bm.swap_in(1)
+    assert [c for c, _ in back] == [0, 1, 2] and bm.num_free_cpu_blocks() == 5
+    t1b, n = bm.block_table(1)
+    assert n == 10 and list(t1b) == [g for _, g in back]
+    assert bm.append_tokens(1, [10, 11]) == []  # resident again, private tail
 
-    def __init__(self, num_blocks, bs, prefix_cache, rng):
+
+def test_swap_out_leaves_shared_blocks_to_their_other_holders():
+    bs = 4
+    bm = B.BlockManager(8, bs)
+    bm.set_cpu_blocks(8)
+    bm.add_sequence(1, list(range(6)))  # blocks 0 (full), 1 (half)
+    bm.fork(1, 2)
+    copies = bm.swap_out(1)
+    assert [g for g, _ in copies] == [0, 1]
+    assert [bm.ref_count(b) for b in (0, 1)] == [1, 1]  # still held by the child
+    assert list(bm.block_table(2)[0]) == [0, 1]
+    assert bm.append_tokens(2, [6]) == []  # the child's tail is private now
+    bm.free_sequence(1)  # frees the swapped sequence's slots
+    assert bm.num_free_cpu_blocks() == 8
+
+
+def test_swap_refusals_change_nothing():
+    bs = 4
+    bm = B.BlockManager(8, bs)
+    bm.set_cpu_blocks(2)
+    bm.add_sequence(1, list(range(12)))  # 3 blocks, 2 slots
+    free = bm.num_free_blocks()
+    with pytest.raises(B.PagedAttnError) as e:
+        bm.swap_out(1)
+    assert e.value.status == 3 and bm.num_free_cpu_blocks() == 2 and bm.num_free_blocks() == free
+    assert bm.block_table(1)[1] == 12
+    with pytest.raises(B.PagedAttnError):
+        bm.swap_in(1)  # not swapped out
+    bm.add_sequence(2, [1, 2])
+    bm.swap_out(2)
+    with pytest.raises(B.PagedAttnError):
+        bm.set_cpu_blocks(10)  # a slot is in use
+    bm.swap_in(2)
+    bm.set_cpu_blocks(10)
+    assert bm.num_free_cpu_blocks() == 10
+
+
+def test_prefix_cache_survives_a_swap_out():
+    """Swapping a sequence out releases its blocks; full cached blocks stay in
+    the prefix cache (their KV is still on the GPU) until reused."""
+    bs = 4
+    bm = B.BlockManager(16, bs)
+    bm.set_cpu_blocks(4)
+    prompt = list(range(100, 109))  # 2 full blocks + 1 token
+    bm.add_sequence(1, prompt)
+    bm.swap_out(1)
+    assert bm.add_sequence(2, prompt) == 8
+
+
+class _Caller:
+    """A caller of the manager with a simulated KV store (token ids) and a
+    host swap tier."""
+
+    def __init__(self, num_blocks, bs, prefix_cache, rng, cpu_blocks=0):
         self.bm = B.BlockManager(num_blocks, bs, prefix_cache)
-        self.bs, self.nb, self.rng = bs, num_blocks, rng
+        self.bm.set_cpu_blocks(cpu_blocks)
+        self.bs, self.nb, self.rng, self.ncpu = bs, num_blocks, rng, cpu_blocks
         self.store = np.full((num_blocks, bs), -1, dtype=np.int64)
+        self.cpu_store = np.full((max(cpu_blocks, 1), bs), -1, dtype=np.int64)
         self.seqs = {}  # id -> list of token ids
+        self.swapped = set()
         self.next_id = 0
 
     def _write(self, sid, start, toks):
@@ -153,6 +234,27 @@ class _Caller:
         self._write(sid, cached, prompt[cached:])
         self.seqs[sid] = list(prompt)
 
+    def swap_out(self, sid):
+        try:
+            copies = self.bm.swap_out(sid)
+        except B.PagedAttnError as e:
+            assert e.status == 3
+            return
+        for g, c in copies:
+            self.cpu_store[c] = self.store[g]
+        self.swapped.add(sid)
+
+    def swap_in(self, sid):
+        try:
+            copies = self.bm.swap_in(sid)
+        except B.PagedAttnError as e:
+            assert e.status == 3
+            return
+        for c, g in copies:
+            assert self.bm.ref_count(g) == 1
+            self.store[g] = self.cpu_store[c]
+        self.swapped.discard(sid)
+
     def fork(self, parent):
         sid = self.next_id
         self.next_id += 1
@@ -173,10 +275,22 @@ class _Caller:
     def free(self, sid):
         self.bm.free_sequence(sid)
         del self.seqs[sid]
+        self.swapped.discard(sid)
 
     def check(self):
-        held = {}
+        held, slots = {}, []
+        for sid in self.swapped:
+            toks = self.seqs[sid]
+            sl = self.bm.swapped_slots(sid)
+            assert len(sl) == -(-len(toks) // self.bs)
+            got = [int(self.cpu_store[sl[i // self.bs], i % self.bs]) for i in range(len(toks))]
+            assert got == toks, f"swapped sequence {sid} reads back wrong tokens"
+            slots += sl
+        assert len(set(slots)) == len(slots), "a host slot held twice"
+        assert self.bm.num_free_cpu_blocks() + len(slots) == self.ncpu
         for sid, toks in self.seqs.items():
+            if sid in self.swapped:
+                continue
             table, n = self.bm.block_table(sid)
             assert n == len(toks)
             got = [int(self.store[table[i // self.bs], i % self.bs]) for i in range(n)]
@@ -188,17 +302,23 @@ class _Caller:
         assert self.bm.num_free_blocks() + len(held) == self.nb
 
 
+@pytest.mark.parametrize("swap", [False, True])
 @pytest.mark.parametrize("prefix_cache", [True, False])
 @pytest.mark.parametrize("seed", range(6))
-def test_randomized_against_a_simulated_store(seed, prefix_cache):
+def test_randomized_against_a_simulated_store(seed, prefix_cache, swap):
     rng = np.random.default_rng(seed)
     bs = int(rng.choice([2, 4, 16]))
-    c = _Caller(int(rng.integers(8, 64)), bs, prefix_cache, rng)
+    c = _Caller(int(rng.integers(8, 64)), bs, prefix_cache, rng,
+                cpu_blocks=int(rng.integers(4, 48)) if swap else 0)
     prompts = [list(rng.integers(0, 3, size=int(rng.integers(1, 5 * bs)))) for _ in range(6)]
     for _ in range(400):
         op = rng.random()
-        live = list(c.seqs)
-        if op < 0.3 or not live:
+        live = [s for s in c.seqs if s not in c.swapped]
+        if swap and c.swapped and op < 0.1:
+            c.swap_in(sorted(c.swapped)[int(rng.integers(len(c.swapped)))])
+        elif swap and live and op < 0.2:
+            c.swap_out(live[int(rng.integers(len(live)))])
+        elif op < 0.3 or not live:
             base = prompts[int(rng.integers(len(prompts)))]
             cut = int(rng.integers(1, len(base) + 1))
             tail = list(rng.integers(0, 3, size=int(rng.integers(0, 2 * bs))))
@@ -209,7 +329,8 @@ def test_randomized_against_a_simulated_store(seed, prefix_cache):
             sid = live[int(rng.integers(len(live)))]
             c.append(sid, [int(x) for x in rng.integers(0, 3, size=int(rng.integers(1, bs + 2)))])
         else:
-            c.free(live[int(rng.integers(len(live)))])
+            everyone = list(c.seqs)
+            c.free(everyone[int(rng.integers(len(everyone)))])
         c.check()
     for sid in list(c.seqs):
         c.free(sid)
