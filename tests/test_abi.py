@@ -56,3 +56,25 @@ def test_null_pool_arguments(lib):
     assert lib.pa_pool_set_unit_cost(None, 0) == 1
     f = ctypes.c_uint32()
     assert lib.pa_get_device_error(None, None, ctypes.byref(f)) == 1
+    i = (ctypes.c_int32 * 1)(0)
+    assert lib.pa_copy_blocks(None, i, i, 1, None) == 1
+    assert lib.pa_swap_blocks(None, i, 1, i, i, 1, 0, None) == 1
+    assert lib.pa_pool_block_bytes(None) == 0
+
+
+def test_null_block_manager_arguments(lib):
+    i = (ctypes.c_int32 * 4)()
+    n = ctypes.c_int32()
+    assert lib.pa_bm_create(0, 16, 1, ctypes.byref(ctypes.c_void_p())) == 1
+    assert lib.pa_bm_create(4, 16, 1, None) == 1
+    assert lib.pa_bm_destroy(None) == 0
+    assert lib.pa_bm_add_sequence(None, 1, None, 0, None) == 1
+    assert lib.pa_bm_fork(None, 1, 2) == 1
+    assert lib.pa_bm_append_tokens(None, 1, None, 1, i, i, 1, ctypes.byref(n)) == 1
+    assert lib.pa_bm_free_sequence(None, 1) == 1
+    assert lib.pa_bm_block_table(None, 1, i, 4, None, None) == 1
+    assert lib.pa_bm_num_free_blocks(None) == 0 and lib.pa_bm_ref_count(None, 0) == -1
+    assert lib.pa_bm_set_cpu_blocks(None, 4) == 1 and lib.pa_bm_num_free_cpu_blocks(None) == 0
+    assert lib.pa_bm_swap_out(None, 1, i, i, 4, ctypes.byref(n)) == 1
+    assert lib.pa_bm_swap_in(None, 1, i, i, 4, ctypes.byref(n)) == 1
+    assert lib.pa_bm_swapped_slots(None, 1, i, 4, ctypes.byref(n)) == 1
