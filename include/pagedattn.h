@@ -229,6 +229,16 @@ PA_API pa_status pa_pool_view(const pa_pool* pool, pa_pool_buffers* out);
  * set, PA_ERR_CUDA if the synchronisation failed, else PA_OK. */
 PA_API pa_status pa_get_device_error(pa_pool* pool, void* stream, uint32_t* flags);
 
+/* Diagnostic of the failure detection: run, on `device`, one bounded device
+ * wait that cannot complete (an mbarrier that nothing arrives at, given up
+ * after about limit_cycles SM clocks, the way every kernel wait of this
+ * library gives up) and return the error bits it recorded in *flags:
+ * PA_DEVERR_TIMEOUT when the wait expired and reported. Synchronous; the
+ * device stays usable afterwards.
+ * Errors: PA_ERR_INVALID_ARG (null flags, device < 0, limit outside
+ * [1, 4e9]; nothing launched), PA_ERR_CUDA. */
+PA_API pa_status pa_selftest_wait_timeout(int32_t device, int64_t limit_cycles, uint32_t* flags);
+
 /* Static description of a status code. */
 PA_API const char* pa_status_string(pa_status s);
 

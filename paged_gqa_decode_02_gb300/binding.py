@@ -101,6 +101,8 @@ def lib():
         L.pa_bm_ref_count.restype = I32
         L.pa_copy_blocks.argtypes = [P, P, P, I32, P]
         L.pa_copy_blocks.restype = I32
+        L.pa_selftest_wait_timeout.argtypes = [I32, I64, ctypes.POINTER(ctypes.c_uint32)]
+        L.pa_selftest_wait_timeout.restype = I32
         L.pa_pool_block_bytes.argtypes = [P]
         L.pa_pool_block_bytes.restype = ctypes.c_size_t
         L.pa_swap_blocks.argtypes = [P, P, I32, P, P, I32, I32, P]

@@ -58,6 +58,17 @@ __global__ void fill_scales(float* p, size_t pages, int per, size_t stride, floa
     p[(i / per) * stride + i % per] = v;
 }
 
+// Diagnostic: one thread waits, with the kernels' bounded wait, on a fresh
+// mbarrier that nothing ever arrives at, and records the expiry as every
+// kernel wait does.
+__global__ void selftest_bounded_wait(uint32_t* err, long long limit_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  pa::mbar_init(&bar, 1);
+  pa::fence_mbar_init();
+  if (!pa::mbar_wait_bounded(&bar, 0, limit_cycles)) pa::set_error(err, PA_DEVERR_TIMEOUT);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Sets the pool's device current for the duration of a call.
@@ -263,6 +274,29 @@ pa_status pa_swap_blocks(pa_pool* p, void* host_buffer, int32_t num_host_blocks,
                               : cudaMemcpyAsync(dev, hst, bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "block swap copy");
   }
+  return PA_OK;
+}
+
+pa_status pa_selftest_wait_timeout(int32_t device, int64_t limit_cycles, uint32_t* flags) {
+  g_last_error[0] = 0;
+  if (!flags || device < 0 || limit_cycles < 1 || limit_cycles > 4000000000LL)
+    return fail(PA_ERR_INVALID_ARG, "null flags, negative device or limit outside [1, 4e9] cycles%s");
+  *flags = 0;
+  DeviceGuard dg(device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  uint32_t* word = nullptr;
+  cudaError_t e = cudaMalloc(&word, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  e = cudaMemset(word, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) {
+    selftest_bounded_wait<<<1, 32>>>(word, (long long)limit_cycles);
+    e = cudaGetLastError();
+  }
+  uint32_t host = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&host, word, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  cudaFree(word);
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test");
+  *flags = host;
   return PA_OK;
 }
 

@@ -60,6 +60,8 @@ def test_null_pool_arguments(lib):
     assert lib.pa_copy_blocks(None, i, i, 1, None) == 1
     assert lib.pa_swap_blocks(None, i, 1, i, i, 1, 0, None) == 1
     assert lib.pa_pool_block_bytes(None) == 0
+    assert lib.pa_selftest_wait_timeout(0, 0, ctypes.byref(f)) == 1  # refused before any launch
+    assert lib.pa_selftest_wait_timeout(0, 1000, None) == 1
 
 
 def test_null_block_manager_arguments(lib):
