@@ -210,3 +210,38 @@ def test_many_slices_per_sequence(splits, combine, early_plan):
         got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine, early_plan=early_plan)
         H.check_attention(got, ref, f"many slices splits={splits} {path} {combine} early={early_plan}")
     assert g.device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+def test_decode_writes_nothing_outside_out_and_workspace(dt):
+    """Canaries: guard regions before and after the output and the workspace
+    keep their bytes through decodes with many slices, both merge modes and
+    the early plan (a stray write past a slot or row would change them)."""
+    torch = H.torch_mod()
+    seq = [300, 1, 0, 45, 1000, 17, 2]
+    wl = W.make_case(f"canary_{dt}", 77, len(seq), 8, 2, 128, 16, dt, seq, extra_blocks=1,
+                     channel_offset_sigma=None if dt == "bf16" else 0.5)
+    g, o = H.load_both(wl)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
+    assert st == 0
+    B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
+    GW, GO = 4096, 1024  # guard bytes around the workspace, guard floats around out
+    q, table, lens = H.dev(wl.q_bits), H.dev(wl.block_table), H.dev(wl.seq_lens)
+    for splits, combine, early in ((0, "separate", True), (7, "fused", False), (300, "separate", False),
+                                   (1000, "fused", True)):
+        g.set_decode_path("auto", fused_combine=(combine == "fused"), early_plan=early)
+        n = g.workspace_bytes(B, Hq, splits)
+        wbuf = torch.full((n + 2 * GW,), 0xA5, dtype=torch.uint8, device="cuda")
+        ws = wbuf[GW:GW + n]
+        ws.zero_()
+        obuf = torch.full((B * Hq * D + 2 * GO,), 12345.0, dtype=torch.float32, device="cuda")
+        out = obuf[GO:GO + B * Hq * D].view(B, Hq, D)
+        out.fill_(float("nan"))
+        g.decode(q, table, lens, wl.softmax_scale, out=out, workspace=ws, num_splits=splits)
+        torch.cuda.synchronize()
+        what = f"canary {dt} splits={splits} {combine} early={early}"
+        assert bool((wbuf[:GW] == 0xA5).all()) and bool((wbuf[GW + n:] == 0xA5).all()), what + ": workspace guard"
+        assert bool((obuf[:GO] == 12345.0).all()) and bool((obuf[GO + B * Hq * D:] == 12345.0).all()), what + ": out guard"
+        H.check_attention(out.cpu().numpy().reshape(-1, D), ref, what)
+    assert g.device_error() == (0, 0)
+    g.close()
