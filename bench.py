@@ -333,6 +333,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world} (no exchange)"},
         "hbm_gbs": achieved,
         "decode_us": t_dec_max * 1e6,
+        "median_us": {"step": statistics.median(step_ms) * 1e3, "decode": statistics.median(dec_ms) * 1e3},
         "kv_tokens_per_s": world * nb["tokens_scanned"] / t_dec_max,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _traffic(args.workload, args.path),
