@@ -55,6 +55,13 @@ struct Sequence {
   std::vector<int32_t> tail;    // token ids of the partly filled last block (prefix cache)
 };
 
+// Bits of the chain hash kept (all by default). A build with a narrow mask
+// makes collisions frequent, which the tests use to check that a hash hit
+// is only taken after its token ids match.
+#ifndef PA_BM_HASH_MASK
+#define PA_BM_HASH_MASK 0xFFFFFFFFFFFFFFFFull
+#endif
+
 // 64-bit mix (splitmix64 finaliser) and the chain hash of one full block.
 uint64_t mix64(uint64_t x) {
   x += 0x9E3779B97F4A7C15ull;
@@ -66,7 +73,7 @@ uint64_t mix64(uint64_t x) {
 uint64_t block_hash(uint64_t parent, const int32_t* tokens, int32_t n) {
   uint64_t h = mix64(parent ^ 0x5DEECE66Dull);
   for (int32_t i = 0; i < n; ++i) h = mix64(h ^ (uint64_t)(uint32_t)tokens[i]);
-  return h | 1ull;  // never 0 (0 means "no parent")
+  return (h & PA_BM_HASH_MASK) | 1ull;  // never 0 (0 means "no parent")
 }
 
 }  // namespace
