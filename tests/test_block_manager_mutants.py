@@ -47,7 +47,8 @@ MUTANTS = {
 @pytest.fixture(scope="module")
 def objects():
     pbuild.build()
-    objs = [os.path.join(LIB_DIR, f) for f in ("pa_api.o", "pa_append.o", "pa_decode.o")]
+    objs = [os.path.join(LIB_DIR, os.path.splitext(f)[0] + ".o") for f in pbuild.SOURCES
+            if f != "pa_block_manager.cpp"]
     assert all(os.path.exists(o) for o in objs)
     return objs
 
