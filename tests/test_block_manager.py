@@ -335,3 +335,22 @@ def test_randomized_against_a_simulated_store(seed, prefix_cache, swap):
     for sid in list(c.seqs):
         c.free(sid)
     assert c.bm.num_free_blocks() == c.nb
+
+
+def test_copy_on_write_without_room_for_the_copy_is_refused():
+    """An append that needs a copy-on-write copy but is given no room to
+    return it is refused and changes nothing."""
+    import ctypes
+    bs = 4
+    bm = B.BlockManager(8, bs)
+    bm.add_sequence(1, [1, 2, 3, 4, 5, 6])
+    bm.fork(1, 2)
+    before = (list(bm.block_table(2)[0]), bm.num_free_blocks(), bm.ref_count(1))
+    tok = (ctypes.c_int32 * 1)(7)
+    n = ctypes.c_int32(-1)
+    st = B.lib().pa_bm_append_tokens(bm.handle, 2, ctypes.cast(tok, ctypes.c_void_p), 1, None, None, 0,
+                                     ctypes.byref(n))
+    assert st == 1
+    assert (list(bm.block_table(2)[0]), bm.num_free_blocks(), bm.ref_count(1)) == before
+    assert bm.block_table(2)[1] == 6
+    assert bm.append_tokens(2, [7]) == [(1, 2)]  # with room, the copy is returned
