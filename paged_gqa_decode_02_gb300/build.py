@@ -5,6 +5,7 @@ Translation units compile in parallel; the quantising append is built with
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import subprocess
 import sys
@@ -35,7 +36,19 @@ def _newer(target, deps):
 
 
 def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
+    """Compile what is out of date and link the library. Processes that call
+    this at the same time (test workers, ranks) take turns on a lock file, so
+    none links objects another is still writing."""
     os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(verbose, force, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose, force, extra_flags) -> str:
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "pagedattn.h"))
     objs, procs = [], []
