@@ -37,6 +37,8 @@ WORKLOAD_TEXT = {
     "qwen3_8b_int8": "Qwen3-8B-shaped uint8 KV: batch 64, 32 Q / 8 KV heads, head_dim 128, block 16, "
                      "seq_lens U[1,8192]",
     "long_uint4": "long-context uint4 KV: batch 4, 32 Q / 8 KV heads, head_dim 128, block 32, 32768 tokens each",
+    "qwen3_8b_fp8": "Qwen3-8B-shaped fp8 (E4M3) KV: batch 64, 32 Q / 8 KV heads, head_dim 128, block 16, "
+                    "seq_lens U[1,8192]",
     "prefix_mix": "continuous-batching mix with prefix cache: batch 256, 28 Q / 4 KV heads, head_dim 128, "
                   "block 16, lognormal(median 1000) lengths, 8x32 sequences share 512-token prefixes, bf16 KV",
     "tiny": "tiny: batch 2, 4 Q / 2 KV heads, head_dim 64, block 16, seq_lens {37,5}, bf16 KV",
@@ -51,10 +53,12 @@ PROFILE_FOR = {"qwen25_7b_bf16": "profiles/paged_gqa_decode_qwen25_7b_bf16.md",
 # The consumer sections of the decode source each workload's tensor-core
 # kernel compiles from; the other consumers' sections do not reach its code.
 _CONSUMER_SECTIONS = ("consumer math (CUDA cores)", "consumer math (tensor cores)",
-                      "consumer math (tensor cores, uint8 KV)", "consumer math (tensor cores, uint4 KV)")
+                      "consumer math (tensor cores, uint8 KV)", "consumer math (tensor cores, uint4 KV)",
+                      "consumer math (tensor cores, fp8 KV)")
 _USES = {"qwen25_7b_bf16": "consumer math (tensor cores)", "prefix_mix": "consumer math (tensor cores)",
          "qwen3_8b_int8": "consumer math (tensor cores, uint8 KV)",
-         "long_uint4": "consumer math (tensor cores, uint4 KV)"}
+         "long_uint4": "consumer math (tensor cores, uint4 KV)",
+         "qwen3_8b_fp8": "consumer math (tensor cores, fp8 KV)"}
 
 
 _C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)

@@ -22,8 +22,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "pagedattn.h")
 
-PA_KV_BF16, PA_KV_UINT8, PA_KV_UINT4 = 0, 1, 2
-KV_DTYPES = {"bf16": PA_KV_BF16, "uint8": PA_KV_UINT8, "uint4": PA_KV_UINT4}
+PA_KV_BF16, PA_KV_UINT8, PA_KV_UINT4, PA_KV_FP8 = 0, 1, 2, 3
+KV_DTYPES = {"bf16": PA_KV_BF16, "uint8": PA_KV_UINT8, "uint4": PA_KV_UINT4, "fp8": PA_KV_FP8}
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
           4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE_BOUNDS", 6: "PA_ERR_TIMEOUT"}
 DEVERR_BLOCK_TABLE, DEVERR_SEQ_LEN, DEVERR_APPEND, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
@@ -254,13 +254,15 @@ class PagedKVPool:
         if self.kv_dtype == "bf16":
             return {"k": comp(b.k, bs * D * 2, torch.int16).unflatten(2, (bs, D)),
                     "v": comp(b.v, bs * D * 2, torch.int16).unflatten(2, (bs, D))}
-        w = D if self.kv_dtype == "uint8" else D // 2
-        return {"k": comp(b.k, bs * w, torch.uint8).unflatten(2, (bs, w)),
-                "v": comp(b.v, bs * w, torch.uint8).unflatten(2, (bs, w)),
-                "k_scale": comp(b.k_scale, D * 4, torch.float32),
-                "k_zp": comp(b.k_zp, D * 4, torch.int32),
-                "v_scale": comp(b.v_scale, D * 4, torch.float32),
-                "v_zp": comp(b.v_zp, D * 4, torch.int32)}
+        w = D // 2 if self.kv_dtype == "uint4" else D
+        parts = {"k": comp(b.k, bs * w, torch.uint8).unflatten(2, (bs, w)),
+                 "v": comp(b.v, bs * w, torch.uint8).unflatten(2, (bs, w)),
+                 "k_scale": comp(b.k_scale, D * 4, torch.float32),
+                 "v_scale": comp(b.v_scale, D * 4, torch.float32)}
+        if self.kv_dtype != "fp8":  # fp8 pools hold no zero points
+            parts["k_zp"] = comp(b.k_zp, D * 4, torch.int32)
+            parts["v_zp"] = comp(b.v_zp, D * 4, torch.int32)
+        return parts
 
     def copy_blocks(self, src, dst, stream=None):
         """Copy whole blocks src[i] -> dst[i] (copy-on-write of shared blocks)."""

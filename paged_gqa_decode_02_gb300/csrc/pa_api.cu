@@ -89,9 +89,10 @@ struct DeviceGuard {
 // work of a unit (query load, state deposit and merge, row or partial write)
 // in page times of the pool's decode kernel, as measured on GB300 over the
 // Qwen-shaped bf16 and uint8 workloads and the prefix-sharing mix (uint8
-// pages are short to stream and costly to decode, so a unit weighs more).
+// pages are short to stream and costly to decode, so a unit weighs more;
+// fp8 pages, of the same size and decoded the same way, take uint8's value).
 int32_t default_unit_cost(const pa_pool* p) {
-  return p->desc.kv_dtype == PA_KV_UINT8 ? 10 : 6;
+  return p->desc.kv_dtype == PA_KV_UINT8 || p->desc.kv_dtype == PA_KV_FP8 ? 10 : 6;
 }
 
 bool uses_tensor_cores(const pa_pool* p) {
@@ -132,15 +133,18 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
     return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32%s");
   if (d->head_dim != 64 && d->head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128%s");
-  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_UINT8 && d->kv_dtype != PA_KV_UINT4)
+  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_UINT8 && d->kv_dtype != PA_KV_UINT4 &&
+      d->kv_dtype != PA_KV_FP8)
     return fail(PA_ERR_UNSUPPORTED, "unknown kv_dtype%s");
   DeviceGuard dg(d->device);
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
   const size_t pages = (size_t)d->num_blocks * d->num_kv_heads;
-  const size_t elem_bits = d->kv_dtype == PA_KV_BF16 ? 16 : (d->kv_dtype == PA_KV_UINT8 ? 8 : 4);
+  const size_t elem_bits = d->kv_dtype == PA_KV_BF16 ? 16 : (d->kv_dtype == PA_KV_UINT4 ? 4 : 8);
   const size_t codes_bytes = (size_t)d->block_size * d->head_dim * elem_bits / 8;  // one of K or V
-  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : (size_t)d->head_dim * 4;  // one of 4 arrays
-  const size_t stride = 2 * codes_bytes + 4 * meta_bytes;  // one page record
+  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : (size_t)d->head_dim * 4;  // one metadata array
+  // K scale, K zp, V scale, V zp; fp8 pools hold no zero points
+  const int meta_arrays = d->kv_dtype == PA_KV_FP8 ? 2 : 4;
+  const size_t stride = 2 * codes_bytes + meta_arrays * meta_bytes;  // one page record
   const size_t slab = 256 + pages * stride;
   pa_pool* p = new (std::nothrow) pa_pool();
   if (!p) return fail(PA_ERR_OOM, "host allocation failed%s");
@@ -164,7 +168,10 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   p->dev.k_zp = nullptr;
   p->dev.v_scale = nullptr;
   p->dev.v_zp = nullptr;
-  if (meta_bytes) {
+  if (meta_bytes && meta_arrays == 2) {
+    p->dev.k_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes);
+    p->dev.v_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes + meta_bytes);
+  } else if (meta_bytes) {
     p->dev.k_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes);
     p->dev.k_zp = reinterpret_cast<int32_t*>(rec + 2 * codes_bytes + meta_bytes);
     p->dev.v_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes + 2 * meta_bytes);

@@ -78,16 +78,17 @@ __device__ __forceinline__ int unit_span(int pages, int unit_cost) {
 
 template <int KV, int D, int BS>
 struct PageGeom {
-  static constexpr int kElemBits = KV == PA_KV_BF16 ? 16 : (KV == PA_KV_UINT8 ? 8 : 4);
+  static constexpr int kElemBits = KV == PA_KV_BF16 ? 16 : (KV == PA_KV_UINT4 ? 4 : 8);
   static constexpr int kPageBytes = BS * D * kElemBits / 8;      // one of K or V
   static constexpr int kMetaBytes = KV == PA_KV_BF16 ? 0 : D * 4;  // one of scale or zp
-  static constexpr int kStageBytes = 2 * kPageBytes + 4 * kMetaBytes;
-  // offsets inside a stage
+  static constexpr bool kHasZp = KV == PA_KV_UINT8 || KV == PA_KV_UINT4;  // fp8: scales only
+  static constexpr int kStageBytes = 2 * kPageBytes + (kHasZp ? 4 : 2) * kMetaBytes;
+  // offsets inside a stage (the zero-point offsets only where kHasZp)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kPageBytes;
   static constexpr int kOffKs = 2 * kPageBytes;
   static constexpr int kOffKz = kOffKs + kMetaBytes;
-  static constexpr int kOffVs = kOffKz + kMetaBytes;
+  static constexpr int kOffVs = kHasZp ? kOffKz + kMetaBytes : kOffKs + kMetaBytes;
   static constexpr int kOffVz = kOffVs + kMetaBytes;
 };
 
@@ -334,6 +335,12 @@ struct FmaConsumer {
         x[0] = bf16_lo(w);
         x[1] = bf16_hi(w);
       }
+    } else if (KV == PA_KV_FP8) {
+      const uint8_t* row = page + t * D + lane * CPL;
+      const uint32_t w = CPL == 4 ? *reinterpret_cast<const uint32_t*>(row)
+                                  : (uint32_t) * reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) x[c] = e4m3_to_float((w >> (8 * c)) & 0xFF) * sc[c];
     } else {
       uint32_t w;
       if (KV == PA_KV_UINT8) {
@@ -357,14 +364,16 @@ struct FmaConsumer {
     const uint8_t* kp = stage + PG::kOffK;
     const uint8_t* vp = stage + PG::kOffV;
     float ksc[CPL], vsc[CPL];
-    int32_t kzp[CPL], vzp[CPL];
+    int32_t kzp[CPL] = {}, vzp[CPL] = {};
     if (KV != PA_KV_BF16) {
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
         ksc[c] = reinterpret_cast<const float*>(stage + PG::kOffKs)[lane * CPL + c];
-        kzp[c] = reinterpret_cast<const int32_t*>(stage + PG::kOffKz)[lane * CPL + c];
         vsc[c] = reinterpret_cast<const float*>(stage + PG::kOffVs)[lane * CPL + c];
-        vzp[c] = reinterpret_cast<const int32_t*>(stage + PG::kOffVz)[lane * CPL + c];
+        if (PG::kHasZp) {
+          kzp[c] = reinterpret_cast<const int32_t*>(stage + PG::kOffKz)[lane * CPL + c];
+          vzp[c] = reinterpret_cast<const int32_t*>(stage + PG::kOffVz)[lane * CPL + c];
+        }
       }
     }
     // ---- scores
@@ -932,6 +941,256 @@ struct MmaConsumerU8 {
 };
 
 
+// ------------------------------------------------------------------ consumer math (tensor cores, fp8 KV)
+//
+// fp8 (E4M3) pools with head_dim 128: a record (K codes, V codes, K scale,
+// V scale) is staged like a uint8 record, one 2-D TMA box with 128-byte
+// swizzle. The uint8 scheme without zero points: every E4M3 value is an f16
+// value (3 mantissa bits, magnitudes 2^-9 .. 448), so the hardware
+// conversion feeds exact values to the same f16 mma. Scores:
+// s_t = sum_c w_c value_tc with w_c = q_c * scale_c scaled by a power of two
+// and split into an f16 high part and remainder. P.V: raw[c][h] =
+// sum_t value_tc p_th, then o = alpha o + scale_c raw per page. A slot past
+// the sequence end may hold any bit pattern, NaN included, which p = 0
+// would not cancel: its codes are replaced by zero before P.V.
+template <int BS, int G>
+struct MmaConsumerFp8 {
+  static constexpr int D = 128;
+  static constexpr int KS = 8;        // 16-channel k-steps
+  static constexpr int TT = BS / 16;  // 16-token tiles per page
+  static constexpr int ROW = 128;     // bytes per token row
+  static_assert(G <= 8, "head group");
+  using PG = PageGeom<PA_KV_FP8, 128, BS>;
+
+  uint32_t qp[16];  // q[head g] as bf16 pairs: channels 16k + 4q + {0,1} at 2k, {2,3} at 2k+1
+  float o[8][4];    // O^T tile mt = 2p + s: rows -> channels 32p + 4g + 2s + {0, 1}
+  float m0, m1, l0, l1;
+  float scale_log2;
+
+  __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
+    const int lane = threadIdx.x & 31;
+    const int hg = lane >> 2, q4 = (lane & 3) * 4;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      uint2 w = make_uint2(0, 0);
+      if (hg < g) w = *reinterpret_cast<const uint2*>(q_smem + hg * D + 16 * k + q4);
+      qp[2 * k] = w.x;
+      qp[2 * k + 1] = w.y;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][i] = 0.0f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.0f;
+    scale_log2 = sl2;
+  }
+
+  __device__ __forceinline__ static float4 lds_f4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+  }
+
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, q = lane & 3;
+    const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
+    // Swizzled addresses in closed form, as in the uint8 consumer: the stage
+    // base is 1024-aligned and the K scales start on row phase 0, the V
+    // scales on row phase 4 (no zero points between them).
+    static_assert(PG::kOffK == 0 && PG::kOffV % 1024 == 0, "code rows start on an 8-row boundary");
+    static_assert((PG::kOffKs / 128) % 8 == 0 && (PG::kOffVs / 128) % 8 == 4, "metadata row phases");
+    static_assert(PG::kStageBytes % 1024 == 0, "every stage base stays 1024-aligned");
+    const uint32_t bq = sb + 16 * q;                 // K scales
+    const uint32_t bg = sb + 16 * gq;                // V scales
+    const uint32_t bk = sb + 144 * gq + 4 * q;       // K codes, row gq
+    const uint32_t bv = sb + PG::kOffV + 288 * q + 16 * (gq >> 2) + 4 * (gq & 3);  // V codes, row 2q
+
+    // ---- w = q * scale of head gq and its largest magnitude
+    float w[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const float4 sc = lds_f4((bq ^ (16 * (k >> 1))) + PG::kOffKs + 128 * (k >> 1) + 64 * (k & 1));
+      w[4 * k + 0] = bf16_lo(qp[2 * k]) * sc.x;
+      w[4 * k + 1] = bf16_hi(qp[2 * k]) * sc.y;
+      w[4 * k + 2] = bf16_lo(qp[2 * k + 1]) * sc.z;
+      w[4 * k + 3] = bf16_hi(qp[2 * k + 1]) * sc.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(w[4 * k + j]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    ex = ex < 1 ? 1 : ex;
+    int sh = 140 - ex;  // 2^sh * amax lands in [2^13, 2^14)
+    sh = sh < -120 ? -120 : (sh > 120 ? 120 : sh);
+    const float f = __uint_as_float((uint32_t)(127 + sh) << 23);
+    const float finv = __uint_as_float((uint32_t)(127 - sh) << 23);
+
+    // ---- k-steps outermost: B = w * 2^sh split high + remainder, and the
+    // score mma of every 16-token tile
+    float sh_[TT][4], sl_[TT][4];
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sh_[tt][i] = sl_[tt][i] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const float w0 = w[4 * k] * f, w1 = w[4 * k + 1] * f, w2 = w[4 * k + 2] * f, w3 = w[4 * k + 3] * f;
+      const uint32_t bh0 = pack_f16(w0, w1), bh1 = pack_f16(w2, w3);
+      const float2 h01 = unpack_f16(bh0), h23 = unpack_f16(bh1);
+      const uint32_t bl0 = pack_f16(w0 - h01.x, w1 - h01.y), bl1 = pack_f16(w2 - h23.x, w3 - h23.y);
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        const uint32_t ka = (bk ^ (16 * k)) + tt * 16 * ROW;  // rows tt*16 + gq and + 8
+        uint32_t c0, c1;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(ka) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(ka + 8 * ROW) : "memory");
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2(c0);        // channels 16k + 4q + {0, 1}
+        a[1] = e4m3x2_to_f16x2(c1);
+        a[2] = e4m3x2_to_f16x2(c0 >> 16);  // channels 16k + 4q + {2, 3}
+        a[3] = e4m3x2_to_f16x2(c1 >> 16);
+        mma_f16_16816(sh_[tt], a, bh0, bh1);
+        mma_f16_16816(sl_[tt], a, bl0, bl1);
+      }
+    }
+    // heads 2q, 2q+1 of the score fragments: the scale from their lanes
+    const float mul0 = __shfl_sync(0xffffffffu, finv, 8 * q) * scale_log2;
+    const float mul1 = __shfl_sync(0xffffffffu, finv, 8 * q + 4) * scale_log2;
+    // ---- online softmax for heads 2q, 2q+1 (rows past the end selected out)
+    float s[TT][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const bool v0 = tt * 16 + gq < valid, v1 = tt * 16 + gq + 8 < valid;
+      s[tt][0] = v0 ? (sh_[tt][0] + sl_[tt][0]) * mul0 : -INFINITY;
+      s[tt][1] = v0 ? (sh_[tt][1] + sl_[tt][1]) * mul1 : -INFINITY;
+      s[tt][2] = v1 ? (sh_[tt][2] + sl_[tt][2]) * mul0 : -INFINITY;
+      s[tt][3] = v1 ? (sh_[tt][3] + sl_[tt][3]) * mul1 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    uint32_t ph[TT][2], pl[TT][2];
+    float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
+      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      ps0 += p0 + p2;
+      ps1 += p1 + p3;
+      const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
+      const float2 f01 = unpack_f16(h01), f23 = unpack_f16(h23);
+      ph[tt][0] = movmatrix_trans(h01);
+      ph[tt][1] = movmatrix_trans(h23);
+      pl[tt][0] = movmatrix_trans(pack_f16(p0 - f01.x, p1 - f01.y));
+      pl[tt][1] = movmatrix_trans(pack_f16(p2 - f23.x, p3 - f23.y));
+    }
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+    // ---- raw[c][h] = sum_t value_tc p_th
+    const bool tail = valid < BS;  // warp-uniform
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      float raw0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, raw1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint32_t va = bv ^ (32 * pr), vo = va ^ 16;  // rows 2q (+8) and 2q + 1 (+8)
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        uint32_t W0, W1, W2, W3;  // tokens tt*16 + 2q + {0, 1, 8, 9}
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W0) : "r"(va + tt * 16 * ROW) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W1) : "r"(vo + tt * 16 * ROW + ROW) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W2) : "r"(va + tt * 16 * ROW + 8 * ROW) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(W3) : "r"(vo + tt * 16 * ROW + 9 * ROW) : "memory");
+        if (tail) {
+          const int t0 = tt * 16 + 2 * q;
+          W0 = t0 < valid ? W0 : 0u;
+          W1 = t0 + 1 < valid ? W1 : 0u;
+          W2 = t0 + 8 < valid ? W2 : 0u;
+          W3 = t0 + 9 < valid ? W3 : 0u;
+        }
+        const uint32_t u01 = prmt(W0, W1, 0x5140), u23 = prmt(W0, W1, 0x7362);
+        const uint32_t v01 = prmt(W2, W3, 0x5140), v23 = prmt(W2, W3, 0x7362);
+        uint32_t A0[4], A1[4];
+        A0[0] = e4m3x2_to_f16x2(u01);        // channel +0, tokens t0 t1
+        A0[1] = e4m3x2_to_f16x2(u01 >> 16);  // channel +1
+        A0[2] = e4m3x2_to_f16x2(v01);        // channel +0, tokens t2 t3
+        A0[3] = e4m3x2_to_f16x2(v01 >> 16);
+        A1[0] = e4m3x2_to_f16x2(u23);        // channel +2
+        A1[1] = e4m3x2_to_f16x2(u23 >> 16);  // channel +3
+        A1[2] = e4m3x2_to_f16x2(v23);
+        A1[3] = e4m3x2_to_f16x2(v23 >> 16);
+        mma_f16_16816(raw0, A0, ph[tt][0], ph[tt][1]);
+        mma_f16_16816(raw0, A0, pl[tt][0], pl[tt][1]);
+        mma_f16_16816(raw1, A1, ph[tt][0], ph[tt][1]);
+        mma_f16_16816(raw1, A1, pl[tt][0], pl[tt][1]);
+      }
+      // fold: o = alpha o + scale raw (V scales on row phase 4)
+      const float4 sc = lds_f4((bg ^ (16 * (4 ^ pr))) + PG::kOffVs + 128 * pr);  // channels 32pr + 4gq ..
+      float* oa = o[2 * pr];
+      float* ob = o[2 * pr + 1];
+      oa[0] = fmaf(a0, oa[0], sc.x * raw0[0]);
+      oa[1] = fmaf(a1, oa[1], sc.x * raw0[1]);
+      oa[2] = fmaf(a0, oa[2], sc.y * raw0[2]);
+      oa[3] = fmaf(a1, oa[3], sc.y * raw0[3]);
+      ob[0] = fmaf(a0, ob[0], sc.z * raw1[0]);
+      ob[1] = fmaf(a1, ob[1], sc.z * raw1[1]);
+      ob[2] = fmaf(a0, ob[2], sc.w * raw1[2]);
+      ob[3] = fmaf(a1, ob[3], sc.w * raw1[3]);
+    }
+  }
+
+  __device__ __forceinline__ void deposit(float* st_acc, float* st_ml) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, q = lane & 3;
+    float s0 = l0, s1 = l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    const int h0 = 2 * q;
+    if (lane < 4) {
+      if (h0 < G) {
+        st_ml[h0 * 2] = m0;
+        st_ml[h0 * 2 + 1] = s0;
+      }
+      if (h0 + 1 < G) {
+        st_ml[(h0 + 1) * 2] = m1;
+        st_ml[(h0 + 1) * 2 + 1] = s1;
+      }
+    }
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+#pragma unroll
+      for (int sd = 0; sd < 2; ++sd) {
+        const int c = 32 * pr + 4 * gq + 2 * sd;
+        const float* ot = o[2 * pr + sd];
+        if (h0 < G) {
+          st_acc[h0 * D + stash_col<2>(h0, c)] = ot[0];
+          st_acc[h0 * D + stash_col<2>(h0, c + 1)] = ot[2];
+        }
+        if (h0 + 1 < G) {
+          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c)] = ot[1];
+          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c + 1)] = ot[3];
+        }
+      }
+    }
+  }
+  static constexpr int kStashSwz = 2;
+};
+
+
 // ------------------------------------------------------------------ consumer math (tensor cores, uint4 KV)
 //
 // Packed uint4 pools with head_dim 128: like the uint8 consumer, on a page
@@ -1302,7 +1561,9 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       TC,
       typename std::conditional<
           KV == PA_KV_BF16, MmaConsumerBf16<D, BS, G>,
-          typename std::conditional<KV == PA_KV_UINT8, MmaConsumerU8<BS, G>, MmaConsumerU4<BS, G>>::type>::type,
+          typename std::conditional<
+              KV == PA_KV_UINT8, MmaConsumerU8<BS, G>,
+              typename std::conditional<KV == PA_KV_FP8, MmaConsumerFp8<BS, G>, MmaConsumerU4<BS, G>>::type>::type>::type,
       FmaConsumer<KV, D, BS, G>>::type;
   static_assert(!TC || KV == PA_KV_BF16 || D == 128,
                 "tensor-core consumers: bf16 pages, or quantised pages of head_dim 128");
@@ -2154,8 +2415,11 @@ int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bo
                 : kv_dtype == PA_KV_UINT8
                     ? (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_UINT8, true>(head_dim, block_size, group)
                                                        : smem_bytes_kv<PA_KV_UINT8, false>(head_dim, block_size, group))
-                    : (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_UINT4, true>(head_dim, block_size, group)
-                                                       : smem_bytes_kv<PA_KV_UINT4, false>(head_dim, block_size, group));
+                : kv_dtype == PA_KV_UINT4
+                    ? (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_UINT4, true>(head_dim, block_size, group)
+                                                       : smem_bytes_kv<PA_KV_UINT4, false>(head_dim, block_size, group))
+                    : (tensor_cores && head_dim == 128 ? smem_bytes_kv<PA_KV_FP8, true>(head_dim, block_size, group)
+                                                       : smem_bytes_kv<PA_KV_FP8, false>(head_dim, block_size, group));
   const size_t per_sm = 227 * 1024;
   int n = (int)(per_sm / (smem + 1024));
   return n < 1 ? 1 : (n > 4 ? 4 : n);
@@ -2196,6 +2460,7 @@ cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& map
   if (kv_dtype == PA_KV_BF16) return dispatch_kv<PA_KV_BF16>(prm, L, stream);
   if (kv_dtype == PA_KV_UINT8) return dispatch_kv<PA_KV_UINT8>(prm, L, stream);
   if (kv_dtype == PA_KV_UINT4) return dispatch_kv<PA_KV_UINT4>(prm, L, stream);
+  if (kv_dtype == PA_KV_FP8) return dispatch_kv<PA_KV_FP8>(prm, L, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -241,6 +241,15 @@ def qwen3_8b_int8(seed: int = 3) -> Workload:
                      channel_offset_sigma=0.5)
 
 
+def qwen3_8b_fp8(seed: int = 3) -> Workload:
+    """The Qwen3-8B-shaped case (same lengths and values as the uint8 one)
+    stored as fp8 (E4M3) codes."""
+    rng = np.random.default_rng([seed, 0])
+    seq = rng.integers(1, 8193, size=64).astype(np.int32)
+    return make_case("qwen3_8b_fp8", seed, 64, 32, 8, 128, 16, "fp8", seq,
+                     channel_offset_sigma=0.5)
+
+
 def long_uint4(seed: int = 4) -> Workload:
     """batch 4, 32 Q / 8 KV heads, head_dim 128, block 32, 32768 tokens per
     sequence, stored as packed uint4 codes."""
@@ -308,6 +317,7 @@ CONFIGS = {
     "qwen25_7b_bf16": qwen25_7b,
     "qwen3_8b_int8": qwen3_8b_int8,
     "long_uint4": long_uint4,
+    "qwen3_8b_fp8": qwen3_8b_fp8,
     "prefix_mix": prefix_mix,
 }
 
