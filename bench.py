@@ -74,12 +74,12 @@ def _code_only(text):
 
 def kernel_source_hash(workload, decode_src=None, common_src=None):
     """sha256 (16 hex digits) of the code this workload's tensor-core decode
-    kernel is compiled from: the decode and common sources without the
+    kernel is compiled from: the decode-kernel and common sources without the
     sections of the consumers it does not use, comments and blank lines
     removed. The sources default to the files in the tree."""
     import hashlib
     csrc = os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc")
-    src = decode_src if decode_src is not None else open(os.path.join(csrc, "pa_decode.cu")).read()
+    src = decode_src if decode_src is not None else open(os.path.join(csrc, "pa_decode_kernels.cuh")).read()
     common = common_src if common_src is not None else open(os.path.join(csrc, "pa_common.cuh")).read()
     keep = _USES[workload]
     parts = src.split("// " + "-" * 66 + " ")

@@ -46,6 +46,20 @@ int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bo
 // too large for 32-bit row coordinates).
 bool make_pool_maps(int kv_dtype, const PoolDev& pool, PoolMaps& maps);
 
+// Per-format launches (one translation unit each).
+cudaError_t launch_decode_bf16(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                               const int32_t* block_table, const int32_t* seq_lens, float* out,
+                               void* workspace, DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_uint8(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                                const int32_t* block_table, const int32_t* seq_lens, float* out,
+                                void* workspace, DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_uint4(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                                const int32_t* block_table, const int32_t* seq_lens, float* out,
+                                void* workspace, DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                              const int32_t* block_table, const int32_t* seq_lens, float* out,
+                              void* workspace, DecodeLaunch& L, cudaStream_t stream);
+
 // Carve the workspace and launch decode + combine.
 cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& maps, const void* q,
                           const int32_t* block_table, const int32_t* seq_lens, float* out,
