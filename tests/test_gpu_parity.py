@@ -212,7 +212,7 @@ def test_many_slices_per_sequence(splits, combine, early_plan):
     assert g.device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 def test_decode_writes_nothing_outside_out_and_workspace(dt):
     """Canaries: guard regions before and after the output and the workspace
     keep their bytes through decodes with many slices, both merge modes and
