@@ -191,6 +191,29 @@ PA_API pa_status pa_decode_noalloc(pa_pool* pool, const void* q, const int32_t* 
 PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int32_t num_q_heads,
                                  int32_t num_splits);
 
+/* pa_decode_multi: several query tokens per sequence against the paged cache
+ * (chunked prefill, and the draft tokens a speculative step verifies; the
+ * engine article, sections 2.2 and 4.2, mixes prefill chunks into decode
+ * steps, TFFInfer section 9.3 plans speculative decoding).
+ *   q    device bf16 [batch][n_q][num_q_heads][head_dim], 16-byte aligned
+ *   out  device float32 [batch][n_q][num_q_heads][head_dim], 16-byte aligned
+ *   seq_lens counts all n_q new tokens of sequence b (stored before the
+ *   call); query token i attends to the tokens t < seq_lens[b] - (n_q-1-i),
+ *   a zero row where that is <= 0.
+ * Other arguments, errors and the early-plan contract as for pa_decode; the
+ * in-kernel merge option does not apply (partials always go through the
+ * combine kernel). The query tokens of a kv head's group are processed in
+ * column groups of at most 8 (token, head) columns, each reading the
+ * sequence's pages once; n_q == 1 is pa_decode. */
+PA_API pa_status pa_decode_multi(pa_pool* pool, const void* q, const int32_t* block_table,
+                                 const int32_t* seq_lens, int32_t batch, int32_t n_q, int32_t num_q_heads,
+                                 int32_t max_blocks, float softmax_scale, float* out, void* workspace,
+                                 size_t workspace_bytes, int32_t num_splits, void* stream);
+
+/* Bytes of workspace pa_decode_multi needs; 0 on invalid arguments. */
+PA_API size_t pa_decode_multi_workspace_bytes(const pa_pool* pool, int32_t batch, int32_t n_q,
+                                              int32_t num_q_heads, int32_t num_splits);
+
 /* Resolve num_splits = 0 to the partition count pa_decode would use. */
 PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
 

@@ -76,6 +76,9 @@ def lib():
         L.pa_decode.argtypes = [P, P, P, P, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
         L.pa_decode_workspace_bytes.argtypes = [P, I32, I32, I32]
         L.pa_decode_workspace_bytes.restype = SZ
+        L.pa_decode_multi.argtypes = [P, P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
+        L.pa_decode_multi_workspace_bytes.argtypes = [P, I32, I32, I32, I32]
+        L.pa_decode_multi_workspace_bytes.restype = SZ
         L.pa_pool_set_decode_path.argtypes = [P, I32]
         L.pa_pool_set_decode_path.restype = I32
         L.pa_pool_set_unit_cost.argtypes = [P, I32]
@@ -334,6 +337,21 @@ class PagedKVPool:
             workspace = self.workspace(B, Hq, num_splits)
         pa_decode(self.handle, q, block_table, seq_lens, B, Hq, int(block_table.shape[1]),
                   softmax_scale, out, workspace, workspace.numel(), num_splits, stream)
+        return out
+
+    def decode_multi(self, q, block_table, seq_lens, softmax_scale, out=None, num_splits=0, stream=None):
+        """Several query tokens per sequence: q [B, n_q, Hq, D] (bf16 bits);
+        query token i of sequence b sees seq_lens[b] - (n_q - 1 - i) tokens."""
+        B, n_q, Hq, D = q.shape
+        if out is None:
+            out = torch.empty((B, n_q, Hq, D), dtype=torch.float32, device=self.device)
+        n = int(lib().pa_decode_multi_workspace_bytes(self.handle, B, n_q, Hq, int(num_splits)))
+        if B and n == 0:
+            raise PagedAttnError(1, "pa_decode_multi_workspace_bytes refused the shape")
+        ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+        _check(lib().pa_decode_multi(self.handle, _ptr(q), _ptr(block_table), _ptr(seq_lens), int(B), int(n_q),
+                                     int(Hq), int(block_table.shape[1]), float(softmax_scale), _ptr(out),
+                                     _ptr(ws), int(ws.numel()), int(num_splits), _stream(stream)))
         return out
 
     def device_error(self, stream=None):

@@ -140,6 +140,13 @@ struct DecodeParams {
   int max_blocks;
   int unit_cost;                // phantom positions per unit on the cost line
   float scale_log2;
+  // Several query tokens per sequence (kernels built with MQ): `batch`
+  // counts virtual sequences v = b * n_cg + cg, column group cg of sequence
+  // b, whose columns c are query token cg * tpg + c / g_heads and head
+  // c % g_heads of the kv head's group; `group` is tpg * g_heads. q and out
+  // are [B][n_q][Hq][D]. Single-token kernels: n_q = n_cg = tpg = 1,
+  // g_heads = group.
+  int n_q, n_cg, tpg, g_heads;
 };
 
 // ------------------------------------------------------------------ split-KV merge
@@ -240,6 +247,36 @@ __device__ __forceinline__ int seq_len_checked(const DecodeParams& p, int b, boo
     return 0;
   }
   return len;
+}
+
+// Virtual sequence v (see DecodeParams): its sequence, its length, its
+// column count, the q / out row of its column c under kv head j, and the
+// causal lag of its column 0 (query token i sees the tokens t < len -
+// (n_q - 1 - i); the lag of column c is lag0 - c / g_heads).
+template <bool MQ>
+__device__ __forceinline__ int seq_of(const DecodeParams& p, int v) {
+  return MQ ? v / p.n_cg : v;
+}
+template <bool MQ>
+__device__ __forceinline__ int vlen_checked(const DecodeParams& p, int v, bool report) {
+  return seq_len_checked(p, seq_of<MQ>(p, v), report);
+}
+template <bool MQ>
+__device__ __forceinline__ int unit_cols(const DecodeParams& p, int v) {
+  if constexpr (MQ) return min(p.tpg, p.n_q - (v % p.n_cg) * p.tpg) * p.g_heads;
+  return p.group;
+}
+template <bool MQ>
+__device__ __forceinline__ long long unit_row(const DecodeParams& p, int v, int j, int c) {
+  if constexpr (MQ) {
+    const int i = (v % p.n_cg) * p.tpg + c / p.g_heads;
+    return ((long long)(v / p.n_cg) * p.n_q + i) * p.num_q_heads + (long long)j * p.g_heads + c % p.g_heads;
+  }
+  return (long long)v * p.num_q_heads + (long long)j * p.group + c;
+}
+template <bool MQ>
+__device__ __forceinline__ int unit_lag0(const DecodeParams& p, int v) {
+  return MQ ? p.n_q - 1 - (v % p.n_cg) * p.tpg : 0;
 }
 
 // first / last thread block whose slice contains flattened page x
@@ -364,8 +401,12 @@ struct FmaConsumer {
     }
   }
 
-  __device__ __forceinline__ void page(const uint8_t* stage, int valid, float* pbuf) {
+  template <bool MQ = false>
+  __device__ __forceinline__ void page(const uint8_t* stage, int valid, float* pbuf, int to_end = 0) {
     const int lane = threadIdx.x & 31;
+    // tokens this lane's column lane % G sees (several query tokens per
+    // sequence: a causal lag; else the page's count)
+    const int vc = MQ ? min(valid, to_end - lag_c) : valid;
     const uint8_t* kp = stage + PG::kOffK;
     const uint8_t* vp = stage + PG::kOffV;
     float ksc[CPL], vsc[CPL];
@@ -412,7 +453,7 @@ struct FmaConsumer {
         }
       }
       const int t = ch * TOKC + lane / G;
-      s[ch] = t < valid ? part[0] : -INFINITY;
+      s[ch] = t < vc ? part[0] : -INFINITY;
     }
     // ---- online softmax (head lane % G)
     float pmax = s[0];
@@ -421,11 +462,13 @@ struct FmaConsumer {
 #pragma unroll
     for (int off = G; off < 32; off <<= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, off));
     const float m_new = fmaxf(m_run, pmax);
-    const float alpha = exp2f(m_run - m_new);
+    // a column that has seen no token yet keeps an empty state
+    const float m_ref = MQ && m_new == -INFINITY ? 0.0f : m_new;
+    const float alpha = exp2f(m_run - m_ref);
     float psum = 0.0f;
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
-      const float p = exp2f(s[ch] - m_new);
+      const float p = exp2f(s[ch] - m_ref);
       psum += p;
       pbuf[(ch * TOKC + lane / G) * G + lane % G] = p;
     }
@@ -474,6 +517,9 @@ struct FmaConsumer {
         for (int c = 0; c < CPL; ++c) dst[c] = acc[h][c];
     }
   }
+  int lag_c = 0;  // causal lag of this lane's column lane % G
+  // several query tokens per sequence: column c lags lag0 - c / gh tokens
+  __device__ __forceinline__ void set_lags(int lag0, int gh) { lag_c = lag0 - (int)((threadIdx.x & 31) % G) / gh; }
   static constexpr int kStashSwz = 0;
 };
 
@@ -528,7 +574,8 @@ struct MmaConsumerBf16 {
     scale_log2 = sl2;
   }
 
-  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+  template <bool MQ = false>
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*, int to_end = 0) {
     const int lane = threadIdx.x & 31;
     const uint32_t kb = smem_u32(stage);
     const uint32_t vb = kb + HALF_BYTES;  // V rows follow K rows within each half
@@ -550,14 +597,18 @@ struct MmaConsumerBf16 {
     }
     // ---- online softmax for heads 2(t%4) and 2(t%4)+1
     const int tok = lane >> 2;
+    // this lane's columns 2q, 2q+1 see the tokens below lim_a, lim_b (several query
+    // tokens per sequence: causal lags; else both are the page's count)
+    const int lim_a = MQ ? min(valid, to_end - lag_a) : valid, lim_b = MQ ? min(valid, to_end - lag_b) : valid;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const bool v0 = tt * 16 + tok < valid, v1 = tt * 16 + tok + 8 < valid;
+      const bool v0 = tt * 16 + tok < lim_a, v1 = tt * 16 + tok + 8 < lim_a;
+      const bool w0 = tt * 16 + tok < lim_b, w1 = tt * 16 + tok + 8 < lim_b;
       s[tt][0] = v0 ? s[tt][0] * scale_log2 : -INFINITY;
-      s[tt][1] = v0 ? s[tt][1] * scale_log2 : -INFINITY;
+      s[tt][1] = w0 ? s[tt][1] * scale_log2 : -INFINITY;
       s[tt][2] = v1 ? s[tt][2] * scale_log2 : -INFINITY;
-      s[tt][3] = v1 ? s[tt][3] * scale_log2 : -INFINITY;
+      s[tt][3] = w1 ? s[tt][3] * scale_log2 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
       mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
     }
@@ -567,15 +618,18 @@ struct MmaConsumerBf16 {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    // a column that has seen no token yet (several query tokens per
+    // sequence) keeps an empty state instead of forming inf - inf
+    const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
+    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
-      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
+      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
@@ -658,6 +712,13 @@ struct MmaConsumerBf16 {
       }
     }
   }
+  int lag_a = 0, lag_b = 0;  // causal lags of this lane's columns 2q, 2q+1
+  // several query tokens per sequence: column c lags lag0 - c / gh tokens
+  __device__ __forceinline__ void set_lags(int lag0, int gh) {
+    const int q = threadIdx.x & 3;
+    lag_a = lag0 - (2 * q) / gh;
+    lag_b = lag0 - (2 * q + 1) / gh;
+  }
   static constexpr int kStashSwz = 1;
 };
 
@@ -728,7 +789,8 @@ struct MmaConsumerU8 {
     return v;
   }
 
-  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+  template <bool MQ = false>
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*, int to_end = 0) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, q = lane & 3;
     const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
@@ -815,14 +877,18 @@ struct MmaConsumerU8 {
 #pragma unroll
       for (int i = 0; i < 4; ++i) s[tt][i] = sh_[tt][i] + sl_[tt][i];
     // ---- online softmax for heads 2q, 2q+1
+    // this lane's columns 2q, 2q+1 see the tokens below lim_a, lim_b (several query
+    // tokens per sequence: causal lags; else both are the page's count)
+    const int lim_a = MQ ? min(valid, to_end - lag_a) : valid, lim_b = MQ ? min(valid, to_end - lag_b) : valid;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const bool v0 = tt * 16 + gq < valid, v1 = tt * 16 + gq + 8 < valid;
+      const bool v0 = tt * 16 + gq < lim_a, v1 = tt * 16 + gq + 8 < lim_a;
+      const bool w0 = tt * 16 + gq < lim_b, w1 = tt * 16 + gq + 8 < lim_b;
       s[tt][0] = v0 ? (s[tt][0] - bias0) * mul0 : -INFINITY;
-      s[tt][1] = v0 ? (s[tt][1] - bias1) * mul1 : -INFINITY;
+      s[tt][1] = w0 ? (s[tt][1] - bias1) * mul1 : -INFINITY;
       s[tt][2] = v1 ? (s[tt][2] - bias0) * mul0 : -INFINITY;
-      s[tt][3] = v1 ? (s[tt][3] - bias1) * mul1 : -INFINITY;
+      s[tt][3] = w1 ? (s[tt][3] - bias1) * mul1 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
       mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
     }
@@ -832,15 +898,18 @@ struct MmaConsumerU8 {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    // a column that has seen no token yet (several query tokens per
+    // sequence) keeps an empty state instead of forming inf - inf
+    const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
+    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
-      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
+      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
@@ -942,6 +1011,13 @@ struct MmaConsumerU8 {
       }
     }
   }
+  int lag_a = 0, lag_b = 0;  // causal lags of this lane's columns 2q, 2q+1
+  // several query tokens per sequence: column c lags lag0 - c / gh tokens
+  __device__ __forceinline__ void set_lags(int lag0, int gh) {
+    const int q = threadIdx.x & 3;
+    lag_a = lag0 - (2 * q) / gh;
+    lag_b = lag0 - (2 * q + 1) / gh;
+  }
   static constexpr int kStashSwz = 2;
 };
 
@@ -997,7 +1073,8 @@ struct MmaConsumerFp8 {
     return v;
   }
 
-  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+  template <bool MQ = false>
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*, int to_end = 0) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, q = lane & 3;
     const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
@@ -1067,14 +1144,18 @@ struct MmaConsumerFp8 {
     const float mul1 = __shfl_sync(0xffffffffu, finv, 8 * q + 4) * scale_log2;
     // ---- online softmax for heads 2q, 2q+1 (rows past the end selected out)
     float s[TT][4];
+    // this lane's columns 2q, 2q+1 see the tokens below lim_a, lim_b (several query
+    // tokens per sequence: causal lags; else both are the page's count)
+    const int lim_a = MQ ? min(valid, to_end - lag_a) : valid, lim_b = MQ ? min(valid, to_end - lag_b) : valid;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const bool v0 = tt * 16 + gq < valid, v1 = tt * 16 + gq + 8 < valid;
+      const bool v0 = tt * 16 + gq < lim_a, v1 = tt * 16 + gq + 8 < lim_a;
+      const bool w0 = tt * 16 + gq < lim_b, w1 = tt * 16 + gq + 8 < lim_b;
       s[tt][0] = v0 ? (sh_[tt][0] + sl_[tt][0]) * mul0 : -INFINITY;
-      s[tt][1] = v0 ? (sh_[tt][1] + sl_[tt][1]) * mul1 : -INFINITY;
+      s[tt][1] = w0 ? (sh_[tt][1] + sl_[tt][1]) * mul1 : -INFINITY;
       s[tt][2] = v1 ? (sh_[tt][2] + sl_[tt][2]) * mul0 : -INFINITY;
-      s[tt][3] = v1 ? (sh_[tt][3] + sl_[tt][3]) * mul1 : -INFINITY;
+      s[tt][3] = w1 ? (sh_[tt][3] + sl_[tt][3]) * mul1 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
       mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
     }
@@ -1084,15 +1165,18 @@ struct MmaConsumerFp8 {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    // a column that has seen no token yet (several query tokens per
+    // sequence) keeps an empty state instead of forming inf - inf
+    const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
+    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
-      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
+      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
@@ -1192,6 +1276,13 @@ struct MmaConsumerFp8 {
       }
     }
   }
+  int lag_a = 0, lag_b = 0;  // causal lags of this lane's columns 2q, 2q+1
+  // several query tokens per sequence: column c lags lag0 - c / gh tokens
+  __device__ __forceinline__ void set_lags(int lag0, int gh) {
+    const int q = threadIdx.x & 3;
+    lag_a = lag0 - (2 * q) / gh;
+    lag_b = lag0 - (2 * q + 1) / gh;
+  }
   static constexpr int kStashSwz = 2;
 };
 
@@ -1261,7 +1352,8 @@ struct MmaConsumerU4 {
     scale_log2 = sl2;
   }
 
-  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*) {
+  template <bool MQ = false>
+  __device__ __forceinline__ void page(uint8_t* stage, int valid, float*, int to_end = 0) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, q = lane & 3;
     const uint32_t sb = smem_u32(stage);  // the whole record is swizzled
@@ -1360,14 +1452,18 @@ struct MmaConsumerU4 {
 
     // ---- online softmax for heads 2q, 2q+1
     float s[TT][4];
+    // this lane's columns 2q, 2q+1 see the tokens below lim_a, lim_b (several query
+    // tokens per sequence: causal lags; else both are the page's count)
+    const int lim_a = MQ ? min(valid, to_end - lag_a) : valid, lim_b = MQ ? min(valid, to_end - lag_b) : valid;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const bool v0 = tt * 16 + gq < valid, v1 = tt * 16 + gq + 8 < valid;
+      const bool v0 = tt * 16 + gq < lim_a, v1 = tt * 16 + gq + 8 < lim_a;
+      const bool w0 = tt * 16 + gq < lim_b, w1 = tt * 16 + gq + 8 < lim_b;
       s[tt][0] = v0 ? (sh_[tt][0] + sl_[tt][0] - bias0) * mul0 : -INFINITY;
-      s[tt][1] = v0 ? (sh_[tt][1] + sl_[tt][1] - bias1) * mul1 : -INFINITY;
+      s[tt][1] = w0 ? (sh_[tt][1] + sl_[tt][1] - bias1) * mul1 : -INFINITY;
       s[tt][2] = v1 ? (sh_[tt][2] + sl_[tt][2] - bias0) * mul0 : -INFINITY;
-      s[tt][3] = v1 ? (sh_[tt][3] + sl_[tt][3] - bias1) * mul1 : -INFINITY;
+      s[tt][3] = w1 ? (sh_[tt][3] + sl_[tt][3] - bias1) * mul1 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
       mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
     }
@@ -1377,15 +1473,18 @@ struct MmaConsumerU4 {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+    // a column that has seen no token yet (several query tokens per
+    // sequence) keeps an empty state instead of forming inf - inf
+    const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
+    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - n0), p1 = exp2f(s[tt][1] - n1);
-      const float p2 = exp2f(s[tt][2] - n0), p3 = exp2f(s[tt][3] - n1);
+      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
+      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
@@ -1493,6 +1592,13 @@ struct MmaConsumerU4 {
       }
     }
   }
+  int lag_a = 0, lag_b = 0;  // causal lags of this lane's columns 2q, 2q+1
+  // several query tokens per sequence: column c lags lag0 - c / gh tokens
+  __device__ __forceinline__ void set_lags(int lag0, int gh) {
+    const int q = threadIdx.x & 3;
+    lag_a = lag0 - (2 * q) / gh;
+    lag_b = lag0 - (2 * q + 1) / gh;
+  }
   static constexpr int kStashSwz = 3;
 };
 
@@ -1504,10 +1610,13 @@ struct MmaConsumerU4 {
 // heads are computed without branches (rows of heads >= g hold stale values
 // and are not stored), so the loads and exponentials of every head overlap.
 // Not inlined: the decode loop keeps its registers.
-template <int D, int G, int W, int SWZ>
+// With ROWS (column groups of several query tokens) head h is written to
+// row (h / gh) * run + h % gh of o_dst instead of row h.
+template <int D, int G, int W, int SWZ, bool ROWS = false>
 __device__ __noinline__ void merge_stash_warp(const float* __restrict__ st_acc,
                                               const float* __restrict__ st_ml, int g,
-                                              float* __restrict__ o_dst, float* __restrict__ lse_dst) {
+                                              float* __restrict__ o_dst, float* __restrict__ lse_dst,
+                                              int gh = 1, int run = 0) {
   constexpr int CPL = D / 32;
   static_assert(CPL == 2 || CPL == 4, "head_dim 64 or 128");
   static_assert(SWZ < 2 || CPL == 4, "swizzles of bits 0-2 need four channels per lane");
@@ -1545,7 +1654,11 @@ __device__ __noinline__ void merge_stash_warp(const float* __restrict__ st_acc,
     }
     if (h < g) {
       const float inv = Lsum > 0.0f ? __frcp_rn(Lsum) : 0.0f;
-      float* dst = o_dst + h * D + lane * CPL;
+      float* dst;
+      if constexpr (ROWS)
+        dst = o_dst + ((long long)(h / gh) * run + h % gh) * D + lane * CPL;
+      else
+        dst = o_dst + h * D + lane * CPL;
       if constexpr (CPL == 4)
         *reinterpret_cast<float4*>(dst) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
       else
@@ -1555,7 +1668,7 @@ __device__ __noinline__ void merge_stash_warp(const float* __restrict__ st_acc,
   }
 }
 
-template <int KV, int D, int BS, int G, int NS, bool TC>
+template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ>
 __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     paged_gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kConsumerWarps = consumer_warps<KV, TC, BS>();
@@ -1649,7 +1762,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   {
     int part = 0;
     for (int b = tid; b < p.batch; b += kThreads) {
-      const int len = seq_len_checked(p, b, cta == 0);
+      const int len = vlen_checked<MQ>(p, b, cta == 0);
       if (b < kLensSmem) lens_sm[b] = len;
       part += unit_span((len + BS - 1) / BS, p.unit_cost);
     }
@@ -1677,7 +1790,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     int running = 0;
     for (int base = 0; base < p.batch; base += kThreads) {
       const int b = base + tid;
-      const int n = b < p.batch ? unit_span(((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS, p.unit_cost) : 0;
+      const int n = b < p.batch ? unit_span(((b < kLensSmem ? lens_sm[b] : vlen_checked<MQ>(p, b, false)) + BS - 1) / BS, p.unit_cost) : 0;
       int tot;
       const int incl = block_incl_scan(n, warp_tot, tot);
       const long long lo = (long long)(running + incl - n) * Hkv;
@@ -1715,7 +1828,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       int running = 0;
       for (int base = 0; base < p.batch; base += kThreads) {
         const int b = base + tid;
-        const int n = b < p.batch ? unit_span(((b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false)) + BS - 1) / BS, p.unit_cost) : 0;
+        const int n = b < p.batch ? unit_span(((b < kLensSmem ? lens_sm[b] : vlen_checked<MQ>(p, b, false)) + BS - 1) / BS, p.unit_cost) : 0;
         int tot;
         const int incl = block_incl_scan(n, warp_tot, tot);
         if (b < p.batch) p.pre_cost[b] = running + incl - n;
@@ -1724,11 +1837,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       }
     }
     if (p.batch == 0 && tid == 0) p.pre_cost[0] = 0;
-    if (p.fused) {
+    if (!MQ && p.fused) {
       // rows of empty sequences: no slice holds a page of them
       const int row_elems = p.num_q_heads * D;
       for (int b = 0; b < p.batch; ++b) {
-        const int len = b < kLensSmem ? lens_sm[b] : seq_len_checked(p, b, false);
+        const int len = b < kLensSmem ? lens_sm[b] : vlen_checked<MQ>(p, b, false);
         if (len == 0)
           for (int e = tid; e < row_elems; e += kThreads) p.out[(long long)b * row_elems + e] = 0.0f;
       }
@@ -1763,7 +1876,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         const long long bb = b0 + lane;
         const int len = bb >= p.batch ? 0
                         : (lens_cached && bb < kLensSmem) ? lens_sm[bb]
-                                                          : seq_len_checked(p, (int)bb, false);
+                                                          : vlen_checked<MQ>(p, (int)bb, false);
         const int n = (len + BS - 1) / BS;  // real pages per unit
         const int cn = unit_span(n, p.unit_cost);  // its span on the cost line
         int x = cn;
@@ -1871,7 +1984,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
               if (segs[mid].k0 <= k) lo = mid; else hi = mid - 1;
             }
             const Seg& sg = segs[lo];
-            const int phys = p.block_table[(long long)sg.b * p.max_blocks + sg.lp0 + (k - sg.k0)];
+            const int phys = p.block_table[(long long)seq_of<MQ>(p, sg.b) * p.max_blocks + sg.lp0 + (k - sg.k0)];
             v[u] = (phys < 0 || phys >= p.pool.num_blocks) ? -1 : phys * Hkv + sg.h;
           }
         }
@@ -1911,10 +2024,18 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           }
         }
         const Seg& qs = segs[qi];
-        const uint16_t* qsrc = p.q + ((long long)qs.b * p.num_q_heads + (long long)qs.h * g) * D;
         if (abort_flag) {
           mbar_arrive(&qfull[slot]);
+        } else if constexpr (MQ) {
+          // one run of g_heads rows per query token of the column group
+          const int cols = unit_cols<MQ>(p, qs.b);
+          q_issued[slot] = gs;
+          mbar_arrive_expect_tx(&qfull[slot], cols * D * 2);
+          for (int c = 0; c < cols; c += p.g_heads)
+            bulk_g2s(qslots + slot * SM::kQBytes + c * D * 2, p.q + unit_row<MQ>(p, qs.b, qs.h, c) * D,
+                     p.g_heads * D * 2, &qfull[slot], pol);
         } else {
+          const uint16_t* qsrc = p.q + ((long long)qs.b * p.num_q_heads + (long long)qs.h * g) * D;
           q_issued[slot] = gs;
           mbar_arrive_expect_tx(&qfull[slot], g * D * 2);
           bulk_g2s(qslots + slot * SM::kQBytes, qsrc, g * D * 2, &qfull[slot], pol);
@@ -1923,8 +2044,13 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       };
       // the window's q rows -> L2 now, so that a q sent late still lands fast
       for (int qi = lane; qi < nseg; qi += 32) {
-        const uint16_t* qsrc = p.q + ((long long)segs[qi].b * p.num_q_heads + (long long)segs[qi].h * g) * D;
-        prefetch_l2_bulk(qsrc, g * D * 2);
+        if constexpr (MQ) {
+          for (int c = 0; c < unit_cols<MQ>(p, segs[qi].b); c += p.g_heads)
+            prefetch_l2_bulk(p.q + unit_row<MQ>(p, segs[qi].b, segs[qi].h, c) * D, p.g_heads * D * 2);
+        } else {
+          const uint16_t* qsrc = p.q + ((long long)segs[qi].b * p.num_q_heads + (long long)segs[qi].h * g) * D;
+          prefetch_l2_bulk(qsrc, g * D * 2);
+        }
       }
       int qseg = 0;    // segments whose first page the issue has reached
       int q_sent = 0;  // segments whose q has been sent (lane 0's count)
@@ -2003,8 +2129,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           if (lane == 0) set_error(p.pool.err, PA_DEVERR_TIMEOUT);
           abort_flag = 1;
         }
-        if (!(sg.flags & kContPrev))
-          cons.begin_unit(reinterpret_cast<const uint16_t*>(qslots + slot * SM::kQBytes), g, p.scale_log2);
+        if (!(sg.flags & kContPrev)) {
+          cons.begin_unit(reinterpret_cast<const uint16_t*>(qslots + slot * SM::kQBytes), unit_cols<MQ>(p, sg.b),
+                          p.scale_log2);
+          if constexpr (MQ) cons.set_lags(unit_lag0<MQ>(p, sg.b), p.g_heads);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[slot]);
         // my pages: k = k0 + i with k % W == cw
@@ -2020,7 +2149,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           if (okp && stage_flag[stage] == 0) {
             const int lp = sg.lp0 + (k - sg.k0);
             const int valid = min(BS, sg.len - lp * BS);
-            cons.page(stages + (size_t)stage * PG::kStageBytes, valid, pbuf);
+            cons.template page<MQ>(stages + (size_t)stage * PG::kStageBytes, valid, pbuf, sg.len - lp * BS);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
@@ -2067,14 +2196,27 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         }
         ++n_dep;
         const long long row0 = (long long)sg.b * p.num_q_heads + (long long)sg.h * g;
-        if (sg.slot < 0)
+        if constexpr (MQ) {
+          // rows of the column group: g_heads per query token, a token's rows
+          // num_q_heads apart
+          const int cols = unit_cols<MQ>(p, sg.b);
+          if (sg.slot < 0)
+            merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz, true>(
+                stash_acc, stash_ml, cols, p.out + unit_row<MQ>(p, sg.b, sg.h, 0) * D, nullptr, p.g_heads,
+                p.num_q_heads);
+          else
+            merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, cols,
+                                                                    p.part_o + (long long)sg.slot * g * D,
+                                                                    p.part_lse + (long long)sg.slot * g);
+        } else if (sg.slot < 0) {
           merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.out + row0 * D, nullptr);
-        else
+        } else {
           merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.part_o + (long long)sg.slot * g * D,
                                                                   p.part_lse + (long long)sg.slot * g);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(merged);  // the stash may be overwritten
-        if (sg.slot >= 0 && p.fused) {
+        if (!MQ && sg.slot >= 0 && p.fused) {
           // the last slice to finish this unit merges its partials (threadfence
           // reduction: partials are fenced before the ticket is taken)
           __threadfence();
@@ -2138,12 +2280,15 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
 // are inputs the decode kernel never writes); after the wait one round of
 // loads fetches every partial of the unit: a thread owns four channels of
 // one head and issues its loads for all slices back to back.
-template <int D>
+// With MQ (several query tokens per sequence) the units are those of the
+// virtual sequences (see DecodeParams): lengths come from sequence b / n_cg
+// and column c of a unit goes to its own row.
+template <int D, bool MQ = false>
 __global__ void __launch_bounds__(256)
     splitkv_combine_kernel(const int32_t* seq_lens, const int32_t* pre_cost, const float* part_o,
                            const float* part_lse, float* out, int batch, int num_kv_heads, int group,
                            int num_q_heads, int num_ctas, int block_size, int max_blocks, int unit_cost,
-                           int lens_early) {
+                           int lens_early, int n_q = 1, int n_cg = 1, int tpg = 1, int g_heads = 1) {
   constexpr int kMaxSl = 64;  // slices handled from the precomputed mask; more go round again
   __shared__ long long sh_sum[2][8];
   pdl_launch_dependents();
@@ -2158,7 +2303,7 @@ __global__ void __launch_bounds__(256)
       // (invalid lengths count as empty, as in the decode kernel)
       long long all = 0, before = 0;
       for (int x = tid; x < batch; x += blockDim.x) {
-        const int len = seq_lens[x];
+        const int len = seq_lens[MQ ? x / n_cg : x];
         const int np =
             (len < 0 || (long long)len > (long long)max_blocks * block_size) ? 0 : (len + block_size - 1) / block_size;
         const int span = unit_span(np, unit_cost);
@@ -2219,14 +2364,27 @@ __global__ void __launch_bounds__(256)
     unit_slices();
   }
   const long long row0 = (long long)b * num_q_heads + (long long)j * group;
+  // the unit's columns and the output row of column c
+  const int cols = MQ ? min(tpg, n_q - (b % n_cg) * tpg) * g_heads : group;
+  auto out_row = [&](int c) -> long long {
+    if constexpr (MQ) {
+      const int i = (b % n_cg) * tpg + c / g_heads;
+      return ((long long)(b / n_cg) * n_q + i) * num_q_heads + (long long)j * g_heads + c % g_heads;
+    }
+    return row0 + c;
+  };
   if (n == 0) {
-    for (int e = tid; e < group * D; e += blockDim.x) out[row0 * D + e] = 0.0f;
+    if constexpr (MQ) {
+      for (int e = tid; e < cols * D; e += blockDim.x) out[out_row(e / D) * D + e % D] = 0.0f;
+    } else {
+      for (int e = tid; e < group * D; e += blockDim.x) out[row0 * D + e] = 0.0f;
+    }
     return;
   }
   if (usl.first == usl.last) return;
   // this thread's four channels of head h
   const int e0 = tid * 4;
-  if (e0 >= group * D) return;
+  if (e0 >= cols * D) return;
   const int h = e0 / D;
   float M = -INFINITY, W = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   for (long long s0 = usl.first; s0 <= usl.last; s0 += kMaxSl) {
@@ -2269,17 +2427,18 @@ __global__ void __launch_bounds__(256)
     }
   }
   const float inv = W > 0.0f ? 1.0f / W : 0.0f;
-  *reinterpret_cast<float4*>(out + row0 * D + e0) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
+  float* dst = MQ ? out + out_row(h) * D + (e0 - h * D) : out + row0 * D + e0;
+  *reinterpret_cast<float4*>(dst) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
 }
 
-template <int KV, int D, int BS, int G, int NS, bool TC>
+template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ = false>
 cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t stream) {
   using SM = Smem<KV, D, BS, G, NS, consumer_warps<KV, TC, BS>(), TC>;
-  auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC>;
+  auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC, MQ>;
   static std::atomic<unsigned long long> ready_dec{0}, ready_comb{0};  // per instantiation, per device
   cudaError_t e = prepare_kernel(kern, (int)SM::kBytes, ready_dec);
   if (e != cudaSuccess) return e;
-  e = prepare_kernel(splitkv_combine_kernel<D>, 0, ready_comb);
+  e = prepare_kernel(splitkv_combine_kernel<D, MQ>, 0, ready_comb);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2298,10 +2457,11 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   cfg.gridDim = dim3(units);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D>, prm.seq_lens, (const int32_t*)prm.pre_cost,
+  return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D, MQ>, prm.seq_lens, (const int32_t*)prm.pre_cost,
                             (const float*)prm.part_o, (const float*)prm.part_lse, prm.out, prm.batch,
                             prm.pool.num_kv_heads, prm.group, prm.num_q_heads, L.num_ctas, prm.pool.block_size,
-                            prm.max_blocks, prm.unit_cost, prm.early_plan);
+                            prm.max_blocks, prm.unit_cost, prm.early_plan, prm.n_q, prm.n_cg, prm.tpg,
+                            prm.g_heads);
 }
 
 // Stages per consumer warp: as many pages in flight as the shared memory
@@ -2327,6 +2487,8 @@ constexpr int stages_per_warp() {
 template <int KV, int D, int BS, bool TC>
 cudaError_t dispatch_g(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t s) {
   constexpr int W = consumer_warps<KV, TC, BS>();
+  // several query tokens per sequence: column groups of up to 8 columns
+  if (L.n_q > 1) return launch_t<KV, D, BS, 8, stages_per_warp<KV, D, BS, 8, W, TC>(), TC, true>(prm, L, s);
   if (L.group <= 2) return launch_t<KV, D, BS, 2, stages_per_warp<KV, D, BS, 2, W, TC>(), TC>(prm, L, s);
   if (L.group <= 4) return launch_t<KV, D, BS, 4, stages_per_warp<KV, D, BS, 4, W, TC>(), TC>(prm, L, s);
   return launch_t<KV, D, BS, 8, stages_per_warp<KV, D, BS, 8, W, TC>(), TC>(prm, L, s);
@@ -2399,13 +2561,17 @@ cudaError_t launch_decode_kv(const PoolDev& pool, const PoolMaps& maps, const vo
   prm.part_lse = L.part_lse;
   prm.tickets = tickets;
   prm.epoch = L.epoch;
-  prm.fused = L.fused_combine ? 1 : 0;
+  prm.fused = L.fused_combine && L.n_q <= 1 ? 1 : 0;  // no in-kernel merge of column groups
   prm.early_plan = L.early_plan ? 1 : 0;
   prm.batch = L.batch;
   prm.num_q_heads = L.num_q_heads;
   prm.group = L.group;
   prm.max_blocks = L.max_blocks;
   prm.scale_log2 = L.scale_log2;
+  prm.n_q = L.n_q > 1 ? L.n_q : 1;
+  prm.n_cg = L.n_q > 1 ? L.n_cg : 1;
+  prm.tpg = L.n_q > 1 ? L.tpg : 1;
+  prm.g_heads = L.n_q > 1 ? L.g_heads : L.group;
   return dispatch_kv<KV>(prm, L, stream);
 }
 

@@ -24,6 +24,13 @@ struct DecodeLaunch {
   bool early_plan;      // plan before waiting on the preceding kernel
   unsigned long long epoch;  // per-call tag of the merge tickets (40 bits, never 0)
   int unit_cost;        // phantom pages per (sequence, kv head) unit in the partition
+  // several query tokens per sequence (n_q > 1): batch counts virtual
+  // sequences (sequence x column group, n_cg per sequence), group is
+  // tpg * g_heads columns (tpg query tokens x g_heads heads)
+  int n_q;
+  int n_cg;
+  int tpg;
+  int g_heads;
   // workspace carve-up
   int32_t* pre_cost;    // [batch + 1] per-head cost-line prefix of the sequences
   float* part_o;        // [num_ctas + batch*Hkv][group][D]

@@ -18,7 +18,8 @@ real ones.
 
 Random streams: ``numpy.random.default_rng([seed, stream])`` with stream
 0 = sequence lengths, 1 = q, 2 = K, 3 = V, 4 = per-channel offsets,
-5 = physical block permutation. Values are drawn in float32 and rounded to
+5 = physical block permutation, 6 = the queries of several tokens per
+sequence. Values are drawn in float32 and rounded to
 bfloat16 with round-to-nearest-even.
 """
 from __future__ import annotations
@@ -214,6 +215,13 @@ def make_case(name, seed, batch, num_q_heads, num_kv_heads, head_dim, block_size
                     num_blocks, seq_lens, table, q, k, v, tok_off,
                     float(np.float32(softmax_scale)),
                     shared_blocks=np.zeros(batch, np.int32), groups=None)
+
+
+def multi_token_queries(seed: int, batch: int, n_q: int, num_q_heads: int, head_dim: int) -> np.ndarray:
+    """Query rows of several new tokens per sequence (chunked prefill or
+    speculative verification), bf16 bits [batch, n_q, Hq, D] from stream 6."""
+    rng = np.random.default_rng([seed, 6])
+    return f32_to_bf16_bits(rng.standard_normal((batch, n_q, num_q_heads, head_dim), dtype=np.float32))
 
 
 def tiny(seed: int = 1) -> Workload:
