@@ -446,7 +446,8 @@ size_t pa_decode_multi_workspace_bytes(const pa_pool* p, int32_t batch, int32_t 
   int tpg, n_cg;
   multi_groups(n_q, num_q_heads / Hkv, &tpg, &n_cg);
   const int cols = tpg * (num_q_heads / Hkv);
-  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, cols);
+  // the kernel for several query tokens is built for 8 columns
+  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, 8);
   return pa::decode_workspace_bytes(ctas, batch * n_cg, Hkv, cols, p->desc.head_dim);
 }
 
@@ -475,7 +476,8 @@ pa_status pa_decode_multi(pa_pool* p, const void* q, const int32_t* block_table,
   int tpg, n_cg;
   multi_groups(n_q, group, &tpg, &n_cg);
   const int cols = tpg * group;
-  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, cols);
+  // the kernel for several query tokens is built for 8 columns
+  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, 8);
   const size_t need = pa::decode_workspace_bytes(ctas, batch * n_cg, p->desc.num_kv_heads, cols, p->desc.head_dim);
   if (workspace_bytes < need) return fail(PA_ERR_OOM, "workspace smaller than pa_decode_multi_workspace_bytes()%s");
   DeviceGuard dg(p->desc.device);
