@@ -348,7 +348,9 @@ class PagedKVPool:
         n = int(lib().pa_decode_multi_workspace_bytes(self.handle, B, n_q, Hq, int(num_splits)))
         if B and n == 0:
             raise PagedAttnError(1, "pa_decode_multi_workspace_bytes refused the shape")
-        ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+        ws = self._ws
         _check(lib().pa_decode_multi(self.handle, _ptr(q), _ptr(block_table), _ptr(seq_lens), int(B), int(n_q),
                                      int(Hq), int(block_table.shape[1]), float(softmax_scale), _ptr(out),
                                      _ptr(ws), int(ws.numel()), int(num_splits), _stream(stream)))

@@ -16,7 +16,8 @@ ELEM_BITS = {"bf16": 16, "uint8": 8, "uint4": 4, "fp8": 8}
 META_BYTES = {"bf16": 0, "uint8": 16, "uint4": 16, "fp8": 8}
 
 
-def decode_bytes(wl) -> dict:
+def decode_bytes(wl, n_q: int = 1) -> dict:
+    """Byte counts of one decode call (n_q query tokens per sequence)."""
     bs, D, Hkv = wl.block_size, wl.head_dim, wl.num_kv_heads
     bits = ELEM_BITS[wl.kv_dtype]
     # valid tokens per physical block (max over the sequences that use it)
@@ -34,8 +35,8 @@ def decode_bytes(wl) -> dict:
     per_token = 2 * Hkv * D * bits // 8  # K and V, all kv heads
     meta_per_block = Hkv * D * META_BYTES[wl.kv_dtype]
     pages = sum(-(-int(s) // bs) for s in wl.seq_lens)
-    q = wl.batch * wl.num_q_heads * D * 2
-    out = wl.batch * wl.num_q_heads * D * 4
+    q = wl.batch * n_q * wl.num_q_heads * D * 2
+    out = wl.batch * n_q * wl.num_q_heads * D * 4
     tables = pages * 4 + wl.batch * 4
     kv_unique = unique_tokens * per_token + len(valid) * meta_per_block
     kv_logical = logical_tokens * per_token + pages * meta_per_block

@@ -143,14 +143,16 @@ class Workload:
                            np.asarray(cu, np.int32), np.asarray(ctx, np.int32),
                            np.ascontiguousarray(np.stack(tabs).astype(np.int32)))]
 
-    def step_call(self) -> AppendCall:
-        """The decode step's append: the last token of every non-empty sequence."""
+    def step_call(self, n_new: int = 1) -> AppendCall:
+        """The decode step's append: the last token of every non-empty
+        sequence (with n_new > 1: its last n_new tokens, or all it has)."""
         B = self.batch
-        sel = [int(self.tok_off[b]) + int(self.seq_lens[b]) - 1 for b in range(B) if self.seq_lens[b] > 0]
+        cnt = np.minimum(self.seq_lens.astype(np.int64), n_new)
+        sel = [int(self.tok_off[b]) + int(self.seq_lens[b]) - int(cnt[b]) + i for b in range(B) for i in range(int(cnt[b]))]
         k = self.k_bits[sel] if sel else np.zeros((0, self.num_kv_heads, self.head_dim), np.uint16)
         v = self.v_bits[sel] if sel else np.zeros((0, self.num_kv_heads, self.head_dim), np.uint16)
-        cu = np.concatenate([[0], np.cumsum((self.seq_lens > 0).astype(np.int64))]).astype(np.int32)
-        ctx = np.maximum(self.seq_lens - 1, 0).astype(np.int32)
+        cu = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        ctx = (self.seq_lens - cnt).astype(np.int32)
         return AppendCall(np.ascontiguousarray(k), np.ascontiguousarray(v), cu, ctx,
                           np.ascontiguousarray(self.block_table))
 
