@@ -25,12 +25,18 @@ def _paths(dt, head_dim):
 
 
 def _run(g, wl, q, path, splits, early):
+    """Decode into an output with guard regions on both sides (canaries: no
+    row may be written outside the [B, n_q, Hq, D] output)."""
     torch = H.torch_mod()
     g.set_decode_path(path, early_plan=early)
-    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    n, GO = int(np.prod(q.shape)), 1024
+    obuf = torch.full((n + 2 * GO,), 12345.0, dtype=torch.float32, device="cuda")
+    out = obuf[GO:GO + n].view(*q.shape)
+    out.fill_(float("nan"))
     g.decode_multi(H.dev(q), H.dev(wl.block_table), H.dev(wl.seq_lens), wl.softmax_scale, out=out,
                    num_splits=splits)
     torch.cuda.synchronize()
+    assert bool((obuf[:GO] == 12345.0).all()) and bool((obuf[GO + n:] == 12345.0).all()), "output guard"
     return out.cpu().numpy().reshape(-1, wl.head_dim)
 
 
