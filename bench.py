@@ -425,25 +425,28 @@ def run_reference(args):
         return
     wl = W.CONFIGS[args.workload]()
     n_seq = min(args.cpu_seqs, wl.batch)
-    o, sub, rows = _oracle_setup(wl, n_seq)
+    n_q = args.query_tokens
+    qm = None if n_q == 1 else W.multi_token_queries(100, wl.batch, n_q, wl.num_q_heads, wl.head_dim)
+    o, sub, rows = _oracle_setup(wl, n_seq, n_q)
     for _ in range(max(3, args.warmup)):
-        _oracle_step(wl, o, sub, rows)
+        _oracle_step(wl, o, sub, rows, n_q, qm)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step(wl, o, sub, rows)
+        _oracle_step(wl, o, sub, rows, n_q, qm)
         times.append(time.perf_counter() - t0)
         if sum(times) > 120:
             break
     t = statistics.mean(times)
-    v = n_seq / t
+    v = n_seq * n_q / t
     res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
            "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quantisation steps)",
            "data": "synthetic (same seeded workload)",
-           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "query_tokens": n_q},
            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-                            "sample": f"{n_seq} of {wl.batch} sequences per step (all heads), append + decode"},
+                            "sample": f"{n_seq} of {wl.batch} sequences per step (all heads, {n_q} query "
+                                      f"token(s) each), append + decode"},
            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
