@@ -37,6 +37,8 @@ WORKLOAD_TEXT = {
     "qwen3_8b_int8": "Qwen3-8B-shaped uint8 KV: batch 64, 32 Q / 8 KV heads, head_dim 128, block 16, "
                      "seq_lens U[1,8192]",
     "long_uint4": "long-context uint4 KV: batch 4, 32 Q / 8 KV heads, head_dim 128, block 32, 32768 tokens each",
+    "qwen3_8b_fp8": "Qwen3-8B-shaped fp8 (E4M3) KV: batch 64, 32 Q / 8 KV heads, head_dim 128, block 16, "
+                    "seq_lens U[1,8192]",
     "prefix_mix": "continuous-batching mix with prefix cache: batch 256, 28 Q / 4 KV heads, head_dim 128, "
                   "block 16, lognormal(median 1000) lengths, 8x32 sequences share 512-token prefixes, bf16 KV",
     "tiny": "tiny: batch 2, 4 Q / 2 KV heads, head_dim 64, block 16, seq_lens {37,5}, bf16 KV",
@@ -51,10 +53,12 @@ PROFILE_FOR = {"qwen25_7b_bf16": "profiles/paged_gqa_decode_qwen25_7b_bf16.md",
 # The consumer sections of the decode source each workload's tensor-core
 # kernel compiles from; the other consumers' sections do not reach its code.
 _CONSUMER_SECTIONS = ("consumer math (CUDA cores)", "consumer math (tensor cores)",
-                      "consumer math (tensor cores, uint8 KV)", "consumer math (tensor cores, uint4 KV)")
+                      "consumer math (tensor cores, uint8 KV)", "consumer math (tensor cores, uint4 KV)",
+                      "consumer math (tensor cores, fp8 KV)")
 _USES = {"qwen25_7b_bf16": "consumer math (tensor cores)", "prefix_mix": "consumer math (tensor cores)",
          "qwen3_8b_int8": "consumer math (tensor cores, uint8 KV)",
-         "long_uint4": "consumer math (tensor cores, uint4 KV)"}
+         "long_uint4": "consumer math (tensor cores, uint4 KV)",
+         "qwen3_8b_fp8": "consumer math (tensor cores, fp8 KV)"}
 
 
 _C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)
@@ -70,12 +74,12 @@ def _code_only(text):
 
 def kernel_source_hash(workload, decode_src=None, common_src=None):
     """sha256 (16 hex digits) of the code this workload's tensor-core decode
-    kernel is compiled from: the decode and common sources without the
+    kernel is compiled from: the decode-kernel and common sources without the
     sections of the consumers it does not use, comments and blank lines
     removed. The sources default to the files in the tree."""
     import hashlib
     csrc = os.path.join(ROOT, "paged_gqa_decode_02_gb300", "csrc")
-    src = decode_src if decode_src is not None else open(os.path.join(csrc, "pa_decode.cu")).read()
+    src = decode_src if decode_src is not None else open(os.path.join(csrc, "pa_decode_kernels.cuh")).read()
     common = common_src if common_src is not None else open(os.path.join(csrc, "pa_common.cuh")).read()
     keep = _USES[workload]
     parts = src.split("// " + "-" * 66 + " ")
@@ -209,24 +213,34 @@ def run_ours(args):
             a = a.view(np.int16)
         return torch.from_numpy(a).to(dev)
 
-    for c in wl.fill_calls(leave_last=True):
+    # several query tokens per sequence (chunked prefill / speculative
+    # verification): the step appends the last n_q tokens and attends with all
+    n_q = args.query_tokens
+    for c in wl.fill_calls(leave_last=(n_q == 1)):
         pool.append_kv(d(c.k_bits), d(c.v_bits), d(c.cu_new), d(c.ctx_lens), d(c.block_table),
                        max_new_per_seq=c.max_new)
-    step = wl.step_call()
+    step = wl.step_call(n_q)
     st_k, st_v, st_cu, st_ctx = d(step.k_bits), d(step.v_bits), d(step.cu_new), d(step.ctx_lens)
-    table, seq_lens, q = d(wl.block_table), d(wl.seq_lens), d(wl.q_bits)
     B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
-    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    q_bits = wl.q_bits if n_q == 1 else W.multi_token_queries(100, B, n_q, Hq, D)
+    table, seq_lens, q = d(wl.block_table), d(wl.seq_lens), d(q_bits)
+    out = torch.empty(q_bits.shape, dtype=torch.float32, device=dev)
     ws = pool.workspace(B, Hq, args.splits)
     splits_used = pool.num_splits(args.splits)
+
+    def decode_call(q_, table_, lens_):
+        if n_q == 1:
+            pool.decode(q_, table_, lens_, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
+        else:
+            pool.decode_multi(q_, table_, lens_, wl.softmax_scale, out=out, num_splits=args.splits)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def one_step():
         # append then decode back to back, as a decode loop runs them (the
         # decode's planning may overlap the append; see --no-early-plan)
-        pool.append_kv(st_k, st_v, st_cu, st_ctx, table, max_new_per_seq=1)
-        pool.decode(q, table, seq_lens, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
+        pool.append_kv(st_k, st_v, st_cu, st_ctx, table, max_new_per_seq=n_q)
+        decode_call(q, table, seq_lens)
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
@@ -263,7 +277,7 @@ def run_ours(args):
     for i in range(K):
         flush.fill_(1)
         d0[i].record(stream)
-        pool.decode(q, table, seq_lens, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
+        decode_call(q, table, seq_lens)
         d1[i].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -280,8 +294,8 @@ def run_ours(args):
     h_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else
                                 np.ascontiguousarray(v)).pin_memory()
             for k, v in (("k", step.k_bits), ("v", step.v_bits), ("cu", step.cu_new), ("ctx", step.ctx_lens),
-                         ("table", wl.block_table), ("lens", wl.seq_lens), ("q", wl.q_bits))}
-    h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+                         ("table", wl.block_table), ("lens", wl.seq_lens), ("q", q_bits))}
+    h_out = torch.empty(q_bits.shape, dtype=torch.float32).pin_memory()
     d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
     bi = sum(v.numel() * v.element_size() for v in h_in.values())
     bo = h_out.numel() * h_out.element_size()
@@ -294,9 +308,8 @@ def run_ours(args):
         a.record(stream)
         for k in d_in:
             d_in[k].copy_(h_in[k], non_blocking=True)
-        pool.append_kv(d_in["k"], d_in["v"], d_in["cu"], d_in["ctx"], d_in["table"], max_new_per_seq=1)
-        pool.decode(d_in["q"], d_in["table"], d_in["lens"], wl.softmax_scale, out=out, workspace=ws,
-                    num_splits=args.splits)
+        pool.append_kv(d_in["k"], d_in["v"], d_in["cu"], d_in["ctx"], d_in["table"], max_new_per_seq=n_q)
+        decode_call(d_in["q"], d_in["table"], d_in["lens"])
         h_out.copy_(out, non_blocking=True)
         z.record(stream)
         z.synchronize()
@@ -304,12 +317,12 @@ def run_ours(args):
             e2e_ms.append(a.elapsed_time(z))
     t_e2e = _max_over_ranks(dist, statistics.mean(e2e_ms) / 1e3)
 
-    nb = decode_bytes(wl)
+    nb = decode_bytes(wl, n_q)
     peak, peak_kind = _peaks()
     achieved = nb["algorithmic"] / t_dec_max / 1e9
     res = {
         "metric": METRIC,
-        "value": world * B / t_step_max,
+        "value": world * B * n_q / t_step_max,
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -324,8 +337,10 @@ def run_ours(args):
                    "num_q_heads": Hq, "num_kv_heads": wl.num_kv_heads, "head_dim": D,
                    "block_size": wl.block_size, "kv_dtype": wl.kv_dtype,
                    "tokens_cached": nb["tokens_scanned"], "num_splits": splits_used,
-                   "step": "append 1 token/seq (kv_quant_append) + paged_gqa_decode (split-KV merge: "
-                           + args.combine + ")",
+                   "step": (f"append {n_q} token(s)/seq (kv_quant_append) + paged_gqa_decode"
+                            + (f" with {n_q} causal query tokens per sequence" if n_q > 1 else "")
+                            + " (split-KV merge: " + (args.combine if n_q == 1 else "separate") + ")"),
+                   "query_tokens": n_q,
                    "decode_path": args.path,
                    "early_plan": not args.no_early_plan,
                    "unit_cost": args.unit_cost,
@@ -336,61 +351,68 @@ def run_ours(args):
         "median_us": {"step": statistics.median(step_ms) * 1e3, "decode": statistics.median(dec_ms) * 1e3},
         "kv_tokens_per_s": world * nb["tokens_scanned"] / t_dec_max,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic(args.workload, args.path),
+                     "frac": achieved / peak,
+                     "traffic": _traffic(args.workload, args.path) if n_q == 1 else None,
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": nb["algorithmic"],
                      "timed": "pa_decode call (decode kernel + split-KV combine) alone, CUDA events on the "
                               "launch stream, a second pass of K calls after the K timed steps"},
-        "e2e": {"value": world * B / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+        "e2e": {"value": world * B * n_q / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": 3 * K,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seqs)
+        res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seqs, n_q)
     if rank == 0:
         print(json.dumps(res), flush=True)
     pool.close()
 
 
-def _oracle_setup(wl, n_seq):
+def _oracle_setup(wl, n_seq, n_q=1):
     """Oracle pool holding the first n_seq sequences' caches (setup, untimed)."""
     from oracle import oracle
     o = oracle.OraclePool(wl.kv_dtype, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
-    for c in wl.fill_calls(leave_last=True):
+    for c in wl.fill_calls(leave_last=(n_q == 1)):
         o.append_call(c)
-    step = wl.step_call()
+    step = wl.step_call(n_q)
     keep = np.arange(n_seq)
-    rows = np.concatenate([np.arange(b * wl.num_q_heads, (b + 1) * wl.num_q_heads) for b in keep]).astype(np.int64)
+    per = n_q * wl.num_q_heads  # output rows per sequence
+    rows = np.concatenate([np.arange(b * per, (b + 1) * per) for b in keep]).astype(np.int64)
     cu = np.concatenate([[0], np.cumsum(np.diff(step.cu_new)[keep])]).astype(np.int32)
     sel = np.concatenate([np.arange(step.cu_new[b], step.cu_new[b + 1]) for b in keep]).astype(np.int64)
     sub = (step.k_bits[sel], step.v_bits[sel], cu, step.ctx_lens[keep], step.block_table[keep])
     return o, sub, rows
 
 
-def _oracle_step(wl, o, sub, rows):
+def _oracle_step(wl, o, sub, rows, n_q=1, q_multi=None):
     st = o.append(*sub)
-    out, st2 = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    if n_q == 1:
+        out, st2 = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    else:
+        out, st2 = o.decode_multi(q_multi, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
     assert st == 0 and st2 == 0
     return out
 
 
-def cpu_baseline(wl, n_seq):
+def cpu_baseline(wl, n_seq, n_q=1):
     from oracle import oracle
+    from paged_gqa_decode_02_gb300 import workloads as W
     n_seq = min(n_seq, wl.batch)
-    o, sub, rows = _oracle_setup(wl, n_seq)
-    _oracle_step(wl, o, sub, rows)
+    o, sub, rows = _oracle_setup(wl, n_seq, n_q)
+    qm = None if n_q == 1 else W.multi_token_queries(100, wl.batch, n_q, wl.num_q_heads, wl.head_dim)
+    _oracle_step(wl, o, sub, rows, n_q, qm)
     reps, t0 = 0, time.perf_counter()
     while True:
-        _oracle_step(wl, o, sub, rows)
+        _oracle_step(wl, o, sub, rows, n_q, qm)
         reps += 1
         if time.perf_counter() - t0 > 10.0 or reps >= 20:
             break
     t = (time.perf_counter() - t0) / reps
-    return {"value": n_seq / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n_seq} of {wl.batch} sequences (all {wl.num_q_heads} heads each), "
-                      f"append + decode step, mean of {reps} steps"}
+    return {"value": n_seq * n_q / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n_seq} of {wl.batch} sequences (all {wl.num_q_heads} heads and {n_q} query token(s) "
+                      f"each), append + decode step, mean of {reps} steps"}
 
 
 def run_reference(args):
@@ -403,25 +425,28 @@ def run_reference(args):
         return
     wl = W.CONFIGS[args.workload]()
     n_seq = min(args.cpu_seqs, wl.batch)
-    o, sub, rows = _oracle_setup(wl, n_seq)
+    n_q = args.query_tokens
+    qm = None if n_q == 1 else W.multi_token_queries(100, wl.batch, n_q, wl.num_q_heads, wl.head_dim)
+    o, sub, rows = _oracle_setup(wl, n_seq, n_q)
     for _ in range(max(3, args.warmup)):
-        _oracle_step(wl, o, sub, rows)
+        _oracle_step(wl, o, sub, rows, n_q, qm)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step(wl, o, sub, rows)
+        _oracle_step(wl, o, sub, rows, n_q, qm)
         times.append(time.perf_counter() - t0)
         if sum(times) > 120:
             break
     t = statistics.mean(times)
-    v = n_seq / t
+    v = n_seq * n_q / t
     res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
            "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quantisation steps)",
            "data": "synthetic (same seeded workload)",
-           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "query_tokens": n_q},
            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-                            "sample": f"{n_seq} of {wl.batch} sequences per step (all heads), append + decode"},
+                            "sample": f"{n_seq} of {wl.batch} sequences per step (all heads, {n_q} query "
+                                      f"token(s) each), append + decode"},
            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
@@ -441,6 +466,8 @@ def main():
     ap.add_argument("--no-early-plan", action="store_true",
                     help="decode plans only after the append kernel has finished")
     ap.add_argument("--cpu-seqs", type=int, default=1 << 30)
+    ap.add_argument("--query-tokens", type=int, default=1,
+                    help="causal query tokens per sequence (chunked prefill / speculative verification)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -18,6 +18,11 @@
  *    zero_point = round(-min/scale), Q = clamp(round(x/scale)+zp, 0, L),
  *    dequantised as (Q - zp) * scale, with L = 255 (uint8) or 15 (uint4, two
  *    codes per byte) (engine article, sections 2.4, 2.6, 4.4).
+ *  - fp8 KV (TFFInfer section 9.3 names FP8 among the formats to add; the
+ *    pages fix no scheme): E4M3 codes of the OCP 8-bit floating point format
+ *    with one symmetric scale per (block, kv head, channel),
+ *    scale = max|x| / 448, code = E4M3(x / scale) rounded to nearest-even and
+ *    saturated to +-448, dequantised as value(code) * scale.
  *  - Decode attention: for each sequence b and query head h, with KV head
  *    j = h / (Hq / Hkv) (GQA as in "从零实现 C++ LLM 推理引擎", section
  *    "3. GQA"), out = softmax(q . K^T * softmax_scale) . V over the
@@ -34,9 +39,12 @@
  *          V scale float32 [head_dim], V zero point int32 [head_dim]
  *   uint4: as uint8 with codes uint8 [block_size][head_dim/2], channel 2i in
  *          the low nibble and 2i+1 in the high nibble
- * One (scale, zero point) pair per (physical block, kv head, channel).
- * Records start on 256-byte boundaries (record bytes: 2 x codes + 4 x 4 x
- * head_dim for quantised pools, 2 x codes for bf16).
+ *   fp8  : K codes (E4M3 bits) uint8 [block_size][head_dim], V codes likewise,
+ *          then K scale float32 [head_dim], V scale float32 [head_dim]
+ * One (scale, zero point) pair, or one scale for fp8, per (physical block,
+ * kv head, channel). Records start on 256-byte boundaries (record bytes:
+ * 2 x codes + 4 x 4 x head_dim for uint8 / uint4, 2 x codes + 2 x 4 x
+ * head_dim for fp8, 2 x codes for bf16).
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
@@ -54,7 +62,7 @@
 extern "C" {
 #endif
 
-typedef enum { PA_KV_BF16 = 0, PA_KV_UINT8 = 1, PA_KV_UINT4 = 2 } pa_kv_dtype;
+typedef enum { PA_KV_BF16 = 0, PA_KV_UINT8 = 1, PA_KV_UINT4 = 2, PA_KV_FP8 = 3 } pa_kv_dtype;
 
 typedef enum {
   PA_OK = 0,
@@ -86,7 +94,7 @@ typedef struct {
 
 /* Device addresses of page 0's components (layout above); page n's
  * component lies n * page_stride bytes further. Scale and zero-point pointers
- * are NULL for a bf16 pool. */
+ * are NULL for a bf16 pool, zero-point pointers for an fp8 pool. */
 typedef struct {
   void* k;
   void* v;
@@ -123,7 +131,9 @@ PA_API pa_status pa_destroy(pa_pool* pool);
  * tokens enter as float(code - zp) * scale, new ones as their bf16 value;
  * scale = (max-min)/L (or |min|/L, or 1.0, for an empty range),
  * zp = rint(-min/scale) (int32, unclamped), code = clamp(rint(x/scale)+zp, 0, L),
- * all in IEEE fp32. A block written by one sequence must not be written by
+ * all in IEEE fp32. fp8 pools likewise re-quantise from float(value(code)) *
+ * scale and the new values: scale = max|x| / 448 (1.0 when not > 0),
+ * code = E4M3(x / scale), nearest-even, saturated to +-448. A block written by one sequence must not be written by
  * another sequence in the same call. Bad table entries or lengths set the
  * device error word and skip that block or sequence. */
 PA_API pa_status pa_append_kv(pa_pool* pool, const void* k_new, const void* v_new, const int32_t* cu_new,
@@ -180,6 +190,29 @@ PA_API pa_status pa_decode_noalloc(pa_pool* pool, const void* q, const int32_t* 
  * count (0 = the automatic split count); 0 on invalid arguments. */
 PA_API size_t pa_decode_workspace_bytes(const pa_pool* pool, int32_t batch, int32_t num_q_heads,
                                  int32_t num_splits);
+
+/* pa_decode_multi: several query tokens per sequence against the paged cache
+ * (chunked prefill, and the draft tokens a speculative step verifies; the
+ * engine article, sections 2.2 and 4.2, mixes prefill chunks into decode
+ * steps, TFFInfer section 9.3 plans speculative decoding).
+ *   q    device bf16 [batch][n_q][num_q_heads][head_dim], 16-byte aligned
+ *   out  device float32 [batch][n_q][num_q_heads][head_dim], 16-byte aligned
+ *   seq_lens counts all n_q new tokens of sequence b (stored before the
+ *   call); query token i attends to the tokens t < seq_lens[b] - (n_q-1-i),
+ *   a zero row where that is <= 0.
+ * Other arguments, errors and the early-plan contract as for pa_decode; the
+ * in-kernel merge option does not apply (partials always go through the
+ * combine kernel). The query tokens of a kv head's group are processed in
+ * column groups of at most 8 (token, head) columns, each reading the
+ * sequence's pages once; n_q == 1 is pa_decode. */
+PA_API pa_status pa_decode_multi(pa_pool* pool, const void* q, const int32_t* block_table,
+                                 const int32_t* seq_lens, int32_t batch, int32_t n_q, int32_t num_q_heads,
+                                 int32_t max_blocks, float softmax_scale, float* out, void* workspace,
+                                 size_t workspace_bytes, int32_t num_splits, void* stream);
+
+/* Bytes of workspace pa_decode_multi needs; 0 on invalid arguments. */
+PA_API size_t pa_decode_multi_workspace_bytes(const pa_pool* pool, int32_t batch, int32_t n_q,
+                                              int32_t num_q_heads, int32_t num_splits);
 
 /* Resolve num_splits = 0 to the partition count pa_decode would use. */
 PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);

@@ -22,8 +22,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "pagedattn.h")
 
-PA_KV_BF16, PA_KV_UINT8, PA_KV_UINT4 = 0, 1, 2
-KV_DTYPES = {"bf16": PA_KV_BF16, "uint8": PA_KV_UINT8, "uint4": PA_KV_UINT4}
+PA_KV_BF16, PA_KV_UINT8, PA_KV_UINT4, PA_KV_FP8 = 0, 1, 2, 3
+KV_DTYPES = {"bf16": PA_KV_BF16, "uint8": PA_KV_UINT8, "uint4": PA_KV_UINT4, "fp8": PA_KV_FP8}
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
           4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE_BOUNDS", 6: "PA_ERR_TIMEOUT"}
 DEVERR_BLOCK_TABLE, DEVERR_SEQ_LEN, DEVERR_APPEND, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
@@ -76,6 +76,9 @@ def lib():
         L.pa_decode.argtypes = [P, P, P, P, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
         L.pa_decode_workspace_bytes.argtypes = [P, I32, I32, I32]
         L.pa_decode_workspace_bytes.restype = SZ
+        L.pa_decode_multi.argtypes = [P, P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
+        L.pa_decode_multi_workspace_bytes.argtypes = [P, I32, I32, I32, I32]
+        L.pa_decode_multi_workspace_bytes.restype = SZ
         L.pa_pool_set_decode_path.argtypes = [P, I32]
         L.pa_pool_set_decode_path.restype = I32
         L.pa_pool_set_unit_cost.argtypes = [P, I32]
@@ -254,13 +257,15 @@ class PagedKVPool:
         if self.kv_dtype == "bf16":
             return {"k": comp(b.k, bs * D * 2, torch.int16).unflatten(2, (bs, D)),
                     "v": comp(b.v, bs * D * 2, torch.int16).unflatten(2, (bs, D))}
-        w = D if self.kv_dtype == "uint8" else D // 2
-        return {"k": comp(b.k, bs * w, torch.uint8).unflatten(2, (bs, w)),
-                "v": comp(b.v, bs * w, torch.uint8).unflatten(2, (bs, w)),
-                "k_scale": comp(b.k_scale, D * 4, torch.float32),
-                "k_zp": comp(b.k_zp, D * 4, torch.int32),
-                "v_scale": comp(b.v_scale, D * 4, torch.float32),
-                "v_zp": comp(b.v_zp, D * 4, torch.int32)}
+        w = D // 2 if self.kv_dtype == "uint4" else D
+        parts = {"k": comp(b.k, bs * w, torch.uint8).unflatten(2, (bs, w)),
+                 "v": comp(b.v, bs * w, torch.uint8).unflatten(2, (bs, w)),
+                 "k_scale": comp(b.k_scale, D * 4, torch.float32),
+                 "v_scale": comp(b.v_scale, D * 4, torch.float32)}
+        if self.kv_dtype != "fp8":  # fp8 pools hold no zero points
+            parts["k_zp"] = comp(b.k_zp, D * 4, torch.int32)
+            parts["v_zp"] = comp(b.v_zp, D * 4, torch.int32)
+        return parts
 
     def copy_blocks(self, src, dst, stream=None):
         """Copy whole blocks src[i] -> dst[i] (copy-on-write of shared blocks)."""
@@ -332,6 +337,23 @@ class PagedKVPool:
             workspace = self.workspace(B, Hq, num_splits)
         pa_decode(self.handle, q, block_table, seq_lens, B, Hq, int(block_table.shape[1]),
                   softmax_scale, out, workspace, workspace.numel(), num_splits, stream)
+        return out
+
+    def decode_multi(self, q, block_table, seq_lens, softmax_scale, out=None, num_splits=0, stream=None):
+        """Several query tokens per sequence: q [B, n_q, Hq, D] (bf16 bits);
+        query token i of sequence b sees seq_lens[b] - (n_q - 1 - i) tokens."""
+        B, n_q, Hq, D = q.shape
+        if out is None:
+            out = torch.empty((B, n_q, Hq, D), dtype=torch.float32, device=self.device)
+        n = int(lib().pa_decode_multi_workspace_bytes(self.handle, B, n_q, Hq, int(num_splits)))
+        if B and n == 0:
+            raise PagedAttnError(1, "pa_decode_multi_workspace_bytes refused the shape")
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+        ws = self._ws
+        _check(lib().pa_decode_multi(self.handle, _ptr(q), _ptr(block_table), _ptr(seq_lens), int(B), int(n_q),
+                                     int(Hq), int(block_table.shape[1]), float(softmax_scale), _ptr(out),
+                                     _ptr(ws), int(ws.numel()), int(num_splits), _stream(stream)))
         return out
 
     def device_error(self, stream=None):

@@ -24,6 +24,10 @@ SOURCES = {
     "pa_api.cu": [],
     "pa_append.cu": ["--fmad=false"],
     "pa_decode.cu": [],
+    "pa_decode_bf16.cu": [],
+    "pa_decode_uint8.cu": [],
+    "pa_decode_uint4.cu": [],
+    "pa_decode_fp8.cu": [],
     "pa_block_manager.cpp": [],
 }
 

@@ -89,9 +89,10 @@ struct DeviceGuard {
 // work of a unit (query load, state deposit and merge, row or partial write)
 // in page times of the pool's decode kernel, as measured on GB300 over the
 // Qwen-shaped bf16 and uint8 workloads and the prefix-sharing mix (uint8
-// pages are short to stream and costly to decode, so a unit weighs more).
+// pages are short to stream and costly to decode, so a unit weighs more;
+// fp8 pages, of the same size and decoded the same way, take uint8's value).
 int32_t default_unit_cost(const pa_pool* p) {
-  return p->desc.kv_dtype == PA_KV_UINT8 ? 10 : 6;
+  return p->desc.kv_dtype == PA_KV_UINT8 || p->desc.kv_dtype == PA_KV_FP8 ? 10 : 6;
 }
 
 bool uses_tensor_cores(const pa_pool* p) {
@@ -132,15 +133,18 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
     return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32%s");
   if (d->head_dim != 64 && d->head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128%s");
-  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_UINT8 && d->kv_dtype != PA_KV_UINT4)
+  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_UINT8 && d->kv_dtype != PA_KV_UINT4 &&
+      d->kv_dtype != PA_KV_FP8)
     return fail(PA_ERR_UNSUPPORTED, "unknown kv_dtype%s");
   DeviceGuard dg(d->device);
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
   const size_t pages = (size_t)d->num_blocks * d->num_kv_heads;
-  const size_t elem_bits = d->kv_dtype == PA_KV_BF16 ? 16 : (d->kv_dtype == PA_KV_UINT8 ? 8 : 4);
+  const size_t elem_bits = d->kv_dtype == PA_KV_BF16 ? 16 : (d->kv_dtype == PA_KV_UINT4 ? 4 : 8);
   const size_t codes_bytes = (size_t)d->block_size * d->head_dim * elem_bits / 8;  // one of K or V
-  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : (size_t)d->head_dim * 4;  // one of 4 arrays
-  const size_t stride = 2 * codes_bytes + 4 * meta_bytes;  // one page record
+  const size_t meta_bytes = d->kv_dtype == PA_KV_BF16 ? 0 : (size_t)d->head_dim * 4;  // one metadata array
+  // K scale, K zp, V scale, V zp; fp8 pools hold no zero points
+  const int meta_arrays = d->kv_dtype == PA_KV_FP8 ? 2 : 4;
+  const size_t stride = 2 * codes_bytes + meta_arrays * meta_bytes;  // one page record
   const size_t slab = 256 + pages * stride;
   pa_pool* p = new (std::nothrow) pa_pool();
   if (!p) return fail(PA_ERR_OOM, "host allocation failed%s");
@@ -164,7 +168,10 @@ pa_status pa_create_pool(const pa_pool_desc* d, pa_pool** out) {
   p->dev.k_zp = nullptr;
   p->dev.v_scale = nullptr;
   p->dev.v_zp = nullptr;
-  if (meta_bytes) {
+  if (meta_bytes && meta_arrays == 2) {
+    p->dev.k_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes);
+    p->dev.v_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes + meta_bytes);
+  } else if (meta_bytes) {
     p->dev.k_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes);
     p->dev.k_zp = reinterpret_cast<int32_t*>(rec + 2 * codes_bytes + meta_bytes);
     p->dev.v_scale = reinterpret_cast<float*>(rec + 2 * codes_bytes + 2 * meta_bytes);
@@ -418,6 +425,82 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
                                     workspace, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode launch");
+  return PA_OK;
+}
+
+// Column groups of several query tokens: tokens per group (as many whole
+// tokens' heads as fit in 8 columns) and groups per sequence.
+static void multi_groups(int n_q, int group, int* tpg, int* n_cg) {
+  int t = 8 / group;
+  if (t < 1) t = 1;
+  if (t > n_q) t = n_q;
+  *tpg = t;
+  *n_cg = (n_q + t - 1) / t;
+}
+
+size_t pa_decode_multi_workspace_bytes(const pa_pool* p, int32_t batch, int32_t n_q, int32_t num_q_heads,
+                                       int32_t num_splits) {
+  if (!p || batch < 0 || n_q < 1 || num_q_heads < 1 || num_splits < 0) return 0;
+  const int Hkv = p->desc.num_kv_heads;
+  if (num_q_heads % Hkv || num_q_heads / Hkv > 8) return 0;
+  int tpg, n_cg;
+  multi_groups(n_q, num_q_heads / Hkv, &tpg, &n_cg);
+  const int cols = tpg * (num_q_heads / Hkv);
+  // the kernel for several query tokens is built for 8 columns
+  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, 8);
+  return pa::decode_workspace_bytes(ctas, batch * n_cg, Hkv, cols, p->desc.head_dim);
+}
+
+pa_status pa_decode_multi(pa_pool* p, const void* q, const int32_t* block_table, const int32_t* seq_lens,
+                          int32_t batch, int32_t n_q, int32_t num_q_heads, int32_t max_blocks,
+                          float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                          int32_t num_splits, void* stream) {
+  g_last_error[0] = 0;
+  if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  if (batch < 0 || max_blocks < 0 || num_splits < 0 || n_q < 1)
+    return fail(PA_ERR_INVALID_ARG, "negative batch, max_blocks or num_splits, or n_q < 1%s");
+  if ((long long)batch * n_q > (1 << 30)) return fail(PA_ERR_INVALID_ARG, "batch * n_q too large%s");
+  if (num_q_heads < 1 || num_q_heads % p->desc.num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads%s");
+  const int group = num_q_heads / p->desc.num_kv_heads;
+  if (group > 8) return fail(PA_ERR_UNSUPPORTED, "GQA group size above 8%s");
+  if (!isfinite(softmax_scale)) return fail(PA_ERR_INVALID_ARG, "softmax_scale is not finite%s");
+  if (batch == 0) return PA_OK;
+  if (!q || !block_table || !seq_lens || !out || !workspace || max_blocks == 0)
+    return fail(PA_ERR_INVALID_ARG, "null device pointer or max_blocks == 0%s");
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned and workspace 256-byte aligned%s");
+  if (n_q == 1)
+    return pa_decode(p, q, block_table, seq_lens, batch, num_q_heads, max_blocks, softmax_scale, out, workspace,
+                     workspace_bytes, num_splits, stream);
+  int tpg, n_cg;
+  multi_groups(n_q, group, &tpg, &n_cg);
+  const int cols = tpg * group;
+  // the kernel for several query tokens is built for 8 columns
+  const int ctas = num_splits > 0 ? num_splits : auto_splits(p, 8);
+  const size_t need = pa::decode_workspace_bytes(ctas, batch * n_cg, p->desc.num_kv_heads, cols, p->desc.head_dim);
+  if (workspace_bytes < need) return fail(PA_ERR_OOM, "workspace smaller than pa_decode_multi_workspace_bytes()%s");
+  DeviceGuard dg(p->desc.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  pa::DecodeLaunch L = {};
+  L.num_ctas = ctas;
+  L.group = cols;
+  L.num_q_heads = num_q_heads;
+  L.batch = batch * n_cg;
+  L.max_blocks = max_blocks;
+  L.scale_log2 = softmax_scale * 1.4426950408889634f;
+  L.tensor_cores = uses_tensor_cores(p);
+  L.fused_combine = false;
+  L.early_plan = p->early_plan;
+  L.epoch = next_epoch();
+  L.unit_cost = p->unit_cost >= 0 ? p->unit_cost : default_unit_cost(p);
+  L.n_q = n_q;
+  L.n_cg = n_cg;
+  L.tpg = tpg;
+  L.g_heads = group;
+  cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
+                                    workspace, L, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode (several query tokens) launch");
   return PA_OK;
 }
 

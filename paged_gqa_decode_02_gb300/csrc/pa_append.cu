@@ -4,7 +4,11 @@
 // 3.6.4: logical token t -> slot t % block_size of block page_table[t /
 // block_size]); the quantiser is the asymmetric per-channel formula of the
 // heterogeneous engine article (section 2.6), applied per (physical block,
-// kv head, channel) as in its section 2.4.
+// kv head, channel) as in its section 2.4. fp8 pools take E4M3 codes (OCP
+// 8-bit floating point) with one symmetric scale max|x| / 448 per (physical
+// block, kv head, channel), rounded to nearest-even and saturated to +-448
+// (the pages name FP8 among the formats to add, TFFInfer section 9.3,
+// without fixing a scheme).
 //
 // This translation unit is compiled with --fmad=false and uses explicitly
 // rounded intrinsics so every fp32 step is one IEEE operation in the stated
@@ -86,6 +90,33 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
       const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
       for (int s = old_cnt; s < valid; ++s)
         dst[s * D + c] = s16[((row0 + s) * Hkv + h) * D + c];
+      continue;
+    }
+
+    if (KV == PA_KV_FP8) {
+      // stored tokens enter as float(value(code)) * scale, new ones as bf16
+      uint8_t* pc = page_of(codes, page, pool.stride);
+      float* psc = page_of(scales, page, pool.stride);
+      const float old_scale = psc[c];
+      float vals[BS];
+      float amax = 0.0f;
+#pragma unroll
+      for (int s = 0; s < BS; ++s) {
+        float x = 0.0f;
+        if (s < old_cnt) {
+          x = __fmul_rn(e4m3_to_float(pc[s * D + c]), old_scale);
+        } else if (s < valid) {
+          x = __bfloat162float(src[((row0 + s) * Hkv + h) * D + c]);
+        }
+        vals[s] = x;
+        if (s < valid && fabsf(x) > amax) amax = fabsf(x);
+      }
+      float scale = __fdiv_rn(amax, 448.0f);
+      if (!(scale > 0.0f)) scale = 1.0f;
+#pragma unroll
+      for (int s = 0; s < BS; ++s)
+        if (s < valid) pc[s * D + c] = float_to_e4m3(__fdiv_rn(vals[s], scale));
+      psc[c] = scale;
       continue;
     }
 
@@ -185,6 +216,8 @@ cudaError_t launch_append(int kv_dtype, const PoolDev& pool, const void* k_new, 
   PA_APPEND_CASE(PA_KV_UINT8, 32)
   PA_APPEND_CASE(PA_KV_UINT4, 16)
   PA_APPEND_CASE(PA_KV_UINT4, 32)
+  PA_APPEND_CASE(PA_KV_FP8, 16)
+  PA_APPEND_CASE(PA_KV_FP8, 32)
 #undef PA_APPEND_CASE
   return cudaErrorInvalidValue;
 }

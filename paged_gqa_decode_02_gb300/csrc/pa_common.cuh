@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -261,6 +262,25 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 __device__ __forceinline__ float2 unpack_f16(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// E4M3 (OCP 8-bit floating point: bias 7, 3 mantissa bits, no infinities,
+// largest finite 448) through the hardware conversions. Every E4M3 value is
+// an f16 value, so widening is exact.
+// Two codes (bits 0-7 and 8-15 of w) -> f16x2 (low half from bits 0-7).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// fp32 -> E4M3, round to nearest-even, saturated to +-448 (finite inputs).
+__device__ __forceinline__ uint8_t float_to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
 }  // namespace pa

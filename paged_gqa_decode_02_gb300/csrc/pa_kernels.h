@@ -24,6 +24,13 @@ struct DecodeLaunch {
   bool early_plan;      // plan before waiting on the preceding kernel
   unsigned long long epoch;  // per-call tag of the merge tickets (40 bits, never 0)
   int unit_cost;        // phantom pages per (sequence, kv head) unit in the partition
+  // several query tokens per sequence (n_q > 1): batch counts virtual
+  // sequences (sequence x column group, n_cg per sequence), group is
+  // tpg * g_heads columns (tpg query tokens x g_heads heads)
+  int n_q;
+  int n_cg;
+  int tpg;
+  int g_heads;
   // workspace carve-up
   int32_t* pre_cost;    // [batch + 1] per-head cost-line prefix of the sequences
   float* part_o;        // [num_ctas + batch*Hkv][group][D]
@@ -45,6 +52,20 @@ int decode_ctas_per_sm(int kv_dtype, int block_size, int head_dim, int group, bo
 // 128 (false if the driver call fails, the shape is not served or the pool is
 // too large for 32-bit row coordinates).
 bool make_pool_maps(int kv_dtype, const PoolDev& pool, PoolMaps& maps);
+
+// Per-format launches (one translation unit each).
+cudaError_t launch_decode_bf16(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                               const int32_t* block_table, const int32_t* seq_lens, float* out,
+                               void* workspace, DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_uint8(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                                const int32_t* block_table, const int32_t* seq_lens, float* out,
+                                void* workspace, DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_uint4(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                                const int32_t* block_table, const int32_t* seq_lens, float* out,
+                                void* workspace, DecodeLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const PoolDev& pool, const PoolMaps& maps, const void* q,
+                              const int32_t* block_table, const int32_t* seq_lens, float* out,
+                              void* workspace, DecodeLaunch& L, cudaStream_t stream);
 
 // Carve the workspace and launch decode + combine.
 cudaError_t launch_decode(int kv_dtype, const PoolDev& pool, const PoolMaps& maps, const void* q,

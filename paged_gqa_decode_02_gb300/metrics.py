@@ -1,8 +1,8 @@
 """Byte accounting for the decode roofline.
 
 Algorithmic bytes of one decode call: K and V of every valid token (codes,
-counted per token, not per page), the scale / zero-point metadata of every
-touched (block, kv head) for quantised pools, q, out, the block-table entries
+counted per token, not per page), the scale (and zero-point) metadata of
+every touched (block, kv head) for quantised pools, q, out, the block-table entries
 read and the sequence lengths. A physical block shared by several sequences
 (prefix cache) is counted once.
 """
@@ -10,10 +10,14 @@ from __future__ import annotations
 
 import numpy as np
 
-ELEM_BITS = {"bf16": 16, "uint8": 8, "uint4": 4}
+ELEM_BITS = {"bf16": 16, "uint8": 8, "uint4": 4, "fp8": 8}
+# metadata bytes per channel of a touched (block, kv head), K and V together:
+# f32 scale + i32 zero point for the integer formats, f32 scale for fp8
+META_BYTES = {"bf16": 0, "uint8": 16, "uint4": 16, "fp8": 8}
 
 
-def decode_bytes(wl) -> dict:
+def decode_bytes(wl, n_q: int = 1) -> dict:
+    """Byte counts of one decode call (n_q query tokens per sequence)."""
     bs, D, Hkv = wl.block_size, wl.head_dim, wl.num_kv_heads
     bits = ELEM_BITS[wl.kv_dtype]
     # valid tokens per physical block (max over the sequences that use it)
@@ -29,10 +33,10 @@ def decode_bytes(wl) -> dict:
                 valid[phys] = v
     unique_tokens = sum(valid.values())
     per_token = 2 * Hkv * D * bits // 8  # K and V, all kv heads
-    meta_per_block = 0 if wl.kv_dtype == "bf16" else 2 * Hkv * D * 8  # f32 scale + i32 zp, K and V
+    meta_per_block = Hkv * D * META_BYTES[wl.kv_dtype]
     pages = sum(-(-int(s) // bs) for s in wl.seq_lens)
-    q = wl.batch * wl.num_q_heads * D * 2
-    out = wl.batch * wl.num_q_heads * D * 4
+    q = wl.batch * n_q * wl.num_q_heads * D * 2
+    out = wl.batch * n_q * wl.num_q_heads * D * 4
     tables = pages * 4 + wl.batch * 4
     kv_unique = unique_tokens * per_token + len(valid) * meta_per_block
     kv_logical = logical_tokens * per_token + pages * meta_per_block

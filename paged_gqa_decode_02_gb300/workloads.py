@@ -18,7 +18,8 @@ real ones.
 
 Random streams: ``numpy.random.default_rng([seed, stream])`` with stream
 0 = sequence lengths, 1 = q, 2 = K, 3 = V, 4 = per-channel offsets,
-5 = physical block permutation. Values are drawn in float32 and rounded to
+5 = physical block permutation, 6 = the queries of several tokens per
+sequence. Values are drawn in float32 and rounded to
 bfloat16 with round-to-nearest-even.
 """
 from __future__ import annotations
@@ -142,14 +143,16 @@ class Workload:
                            np.asarray(cu, np.int32), np.asarray(ctx, np.int32),
                            np.ascontiguousarray(np.stack(tabs).astype(np.int32)))]
 
-    def step_call(self) -> AppendCall:
-        """The decode step's append: the last token of every non-empty sequence."""
+    def step_call(self, n_new: int = 1) -> AppendCall:
+        """The decode step's append: the last token of every non-empty
+        sequence (with n_new > 1: its last n_new tokens, or all it has)."""
         B = self.batch
-        sel = [int(self.tok_off[b]) + int(self.seq_lens[b]) - 1 for b in range(B) if self.seq_lens[b] > 0]
+        cnt = np.minimum(self.seq_lens.astype(np.int64), n_new)
+        sel = [int(self.tok_off[b]) + int(self.seq_lens[b]) - int(cnt[b]) + i for b in range(B) for i in range(int(cnt[b]))]
         k = self.k_bits[sel] if sel else np.zeros((0, self.num_kv_heads, self.head_dim), np.uint16)
         v = self.v_bits[sel] if sel else np.zeros((0, self.num_kv_heads, self.head_dim), np.uint16)
-        cu = np.concatenate([[0], np.cumsum((self.seq_lens > 0).astype(np.int64))]).astype(np.int32)
-        ctx = np.maximum(self.seq_lens - 1, 0).astype(np.int32)
+        cu = np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+        ctx = (self.seq_lens - cnt).astype(np.int32)
         return AppendCall(np.ascontiguousarray(k), np.ascontiguousarray(v), cu, ctx,
                           np.ascontiguousarray(self.block_table))
 
@@ -216,6 +219,13 @@ def make_case(name, seed, batch, num_q_heads, num_kv_heads, head_dim, block_size
                     shared_blocks=np.zeros(batch, np.int32), groups=None)
 
 
+def multi_token_queries(seed: int, batch: int, n_q: int, num_q_heads: int, head_dim: int) -> np.ndarray:
+    """Query rows of several new tokens per sequence (chunked prefill or
+    speculative verification), bf16 bits [batch, n_q, Hq, D] from stream 6."""
+    rng = np.random.default_rng([seed, 6])
+    return f32_to_bf16_bits(rng.standard_normal((batch, n_q, num_q_heads, head_dim), dtype=np.float32))
+
+
 def tiny(seed: int = 1) -> Workload:
     """batch 2, 4 Q / 2 KV heads, head_dim 64, block 16, seq_lens {37, 5},
     a pool of 8 physical blocks (the 4 used ones taken from a seeded
@@ -238,6 +248,15 @@ def qwen3_8b_int8(seed: int = 3) -> Workload:
     rng = np.random.default_rng([seed, 0])
     seq = rng.integers(1, 8193, size=64).astype(np.int32)
     return make_case("qwen3_8b_int8", seed, 64, 32, 8, 128, 16, "uint8", seq,
+                     channel_offset_sigma=0.5)
+
+
+def qwen3_8b_fp8(seed: int = 3) -> Workload:
+    """The Qwen3-8B-shaped case (same lengths and values as the uint8 one)
+    stored as fp8 (E4M3) codes."""
+    rng = np.random.default_rng([seed, 0])
+    seq = rng.integers(1, 8193, size=64).astype(np.int32)
+    return make_case("qwen3_8b_fp8", seed, 64, 32, 8, 128, 16, "fp8", seq,
                      channel_offset_sigma=0.5)
 
 
@@ -308,6 +327,7 @@ CONFIGS = {
     "qwen25_7b_bf16": qwen25_7b,
     "qwen3_8b_int8": qwen3_8b_int8,
     "long_uint4": long_uint4,
+    "qwen3_8b_fp8": qwen3_8b_fp8,
     "prefix_mix": prefix_mix,
 }
 

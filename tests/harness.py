@@ -8,6 +8,7 @@ from oracle import oracle
 from paged_gqa_decode_02_gb300 import workloads as W
 
 BF16_NAN = 0x7FC0
+E4M3_NAN = 0x7F
 ATOL, RTOL = 2e-3, 1e-2  # decode tolerance: max-abs, and per-row max-abs / max|ref|
 
 
@@ -37,22 +38,23 @@ def host_pool_arrays(gpool):
     else:
         out["kc"], out["vc"] = v["k"], v["v"]
         out["ks"], out["vs"] = v["k_scale"], v["v_scale"]
-        out["kz"], out["vz"] = v["k_zp"], v["v_zp"]
+        if "k_zp" in v:
+            out["kz"], out["vz"] = v["k_zp"], v["v_zp"]
     return out
 
 
 def make_pools(wl, poison=True):
     """An empty GPU pool and an empty oracle pool in the same initial state
-    (bf16 pools poisoned with NaN so a stray read shows up)."""
+    (bf16 and fp8 pools poisoned with NaN so a stray read shows up)."""
     from paged_gqa_decode_02_gb300.binding import PagedKVPool
     g = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype)
-    fill = BF16_NAN if (poison and wl.kv_dtype == "bf16") else 0
+    fill = {"bf16": BF16_NAN, "fp8": E4M3_NAN}.get(wl.kv_dtype, 0) if poison else 0
     o = oracle.OraclePool(wl.kv_dtype, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim,
                           fill=fill)
     if fill:
         v = g.view()
-        v["k"].fill_(BF16_NAN)
-        v["v"].fill_(BF16_NAN)
+        v["k"].fill_(fill)
+        v["v"].fill_(fill)
     return g, o
 
 

@@ -54,6 +54,8 @@ def test_null_pool_arguments(lib):
     assert lib.pa_decode_workspace_bytes(None, 1, 4, 0) == 0
     assert lib.pa_destroy(None) == 0
     assert lib.pa_pool_set_unit_cost(None, 0) == 1
+    assert lib.pa_decode_multi(None, None, None, None, 1, 2, 4, 1, 1.0, None, None, 0, 0, None) == 1
+    assert lib.pa_decode_multi_workspace_bytes(None, 1, 2, 4, 0) == 0
     f = ctypes.c_uint32()
     assert lib.pa_get_device_error(None, None, ctypes.byref(f)) == 1
     i = (ctypes.c_int32 * 1)(0)

@@ -2,7 +2,7 @@
 still describes the kernel: the per-workload source hash."""
 import bench
 
-DEC = open(bench.os.path.join(bench.ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_decode.cu")).read()
+DEC = open(bench.os.path.join(bench.ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_decode_kernels.cuh")).read()
 COM = open(bench.os.path.join(bench.ROOT, "paged_gqa_decode_02_gb300", "csrc", "pa_common.cuh")).read()
 SEP = "// " + "-" * 66 + " "
 

@@ -34,7 +34,7 @@ def _copy_oracle_block(o, src, dst):
             a[dst] = a[src]
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 def test_block_manager_tables_drive_append_and_decode(dt):
     bs, Hkv, Hq, D, nb, MB = 16, 2, 8, 128, 48, 8
     rng = np.random.default_rng(11)

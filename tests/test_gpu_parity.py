@@ -38,7 +38,7 @@ def test_tiny_config(splits, path, combine):
     assert g.device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 @pytest.mark.parametrize("seed", range(8))
 def test_random_small(seed, dt):
     wl = W.random_small(seed, dt)
@@ -55,7 +55,7 @@ def test_random_small(seed, dt):
     assert g.device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 @pytest.mark.parametrize("block_size", [16, 32])
 def test_unit_cost_partition(block_size, dt):
     """The cost-balanced partition moves pages between thread blocks but never
@@ -80,7 +80,7 @@ def test_unit_cost_partition(block_size, dt):
         g.set_unit_cost(5000)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 def test_multi_step_tail_requant(dt):
     """Several decode steps, each appending one token per sequence into a
     partly filled block (re-quantised), then attending."""
@@ -155,7 +155,7 @@ def test_host_validation_errors():
     assert e.value.status == 1 and "16-byte" in str(e.value)
 
 
-FULL = ["qwen25_7b_bf16", "qwen3_8b_int8", "long_uint4", "prefix_mix"]
+FULL = ["qwen25_7b_bf16", "qwen3_8b_int8", "long_uint4", "prefix_mix", "qwen3_8b_fp8"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -178,7 +178,7 @@ def test_full_size_config(name):
     assert g.device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "fp8"])
 def test_slices_longer_than_a_window(dt):
     """One or two slices over thousands of pages: a thread block walks its
     slice in several windows and runs continue across window boundaries."""
@@ -212,7 +212,7 @@ def test_many_slices_per_sequence(splits, combine, early_plan):
     assert g.device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 def test_decode_writes_nothing_outside_out_and_workspace(dt):
     """Canaries: guard regions before and after the output and the workspace
     keep their bytes through decodes with many slices, both merge modes and

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 _NAMES = ("k16", "v16", "kc", "vc", "ks", "vs", "kz", "vz")
 
 
-@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4"])
+@pytest.mark.parametrize("dt", ["bf16", "uint8", "uint4", "fp8"])
 def test_swap_out_reuse_and_swap_in(dt):
     torch = H.torch_mod()
     bs, Hkv, Hq, D, nb, MB = 16, 2, 8, 128, 12, 12
