@@ -55,6 +55,14 @@ def make_pools(wl, poison=True):
         v = g.view()
         v["k"].fill_(fill)
         v["v"].fill_(fill)
+    if poison and wl.kv_dtype != "bf16":
+        # scales of never-written blocks are NaN on both sides: a read of one
+        # (a block the append has not quantised yet) shows up in the output
+        v = g.view()
+        v["k_scale"].fill_(float("nan"))
+        v["v_scale"].fill_(float("nan"))
+        o.ks[...] = np.float32(np.nan)
+        o.vs[...] = np.float32(np.nan)
     return g, o
 
 

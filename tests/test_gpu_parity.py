@@ -245,3 +245,27 @@ def test_decode_writes_nothing_outside_out_and_workspace(dt):
         H.check_attention(out.cpu().numpy().reshape(-1, D), ref, what)
     assert g.device_error() == (0, 0)
     g.close()
+
+
+@pytest.mark.parametrize("dt", ["bf16", "uint8"])
+def test_batch_beyond_the_plan_caches(dt):
+    """More sequences than the decode kernel has threads (the plan's multi-pass
+    scan) and than it keeps lengths of in shared memory (later lengths are
+    read again from global memory), with empty and one-token sequences mixed
+    in."""
+    rng = np.random.default_rng([57, 0])
+    seq = rng.integers(0, 40, 5000).astype(np.int32)
+    wl = W.make_case(f"big_batch_{dt}", 57, seq.size, 4, 1, 64, 16, dt, seq,
+                     channel_offset_sigma=None if dt == "bf16" else 0.5)
+    g, o = H.load_both(wl)
+    rows = H.sample_rows(wl, n=256)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    assert st == 0
+    for splits, combine, early in ((0, "separate", True), (97, "fused", False), (3000, "separate", False)):
+        got = H.gpu_decode(g, wl, num_splits=splits, combine=combine, early_plan=early)
+        assert np.isfinite(got).all()
+        H.check_attention(got[rows], ref, f"big batch {dt} splits={splits} {combine}")
+        empty = np.flatnonzero(wl.seq_lens == 0)
+        assert np.all(got.reshape(wl.batch, -1)[empty] == 0)
+    assert g.device_error() == (0, 0)
+    g.close()
