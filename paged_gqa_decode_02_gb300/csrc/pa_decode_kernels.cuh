@@ -157,10 +157,35 @@ struct DecodeParams {
 // out = sum_s w_s o_s / sum_s w_s. Slice i holds a partial of the unit (in
 // slot i + u) iff its page range meets the unit's; slices between the first
 // and last owner can be empty when there are more slices than pages.
+//
+// Cost-line arithmetic. Slice i of G is [T*i/G, T*(i+1)/G) of a line of T
+// positions. When T*G < 2^32 (every launch short of billions of positions)
+// the products and quotients are formed in 32-bit unsigned arithmetic: a
+// 64-bit division is a long software sequence on the GPU, and these sit on
+// the critical path of the planning before the first page is requested.
+__device__ __forceinline__ bool line_small(long long T, long long G) {
+  return T >= 0 && G > 0 && T <= 0xFFFFFFFFLL / G;
+}
+// first position of slice i (0 <= i <= G)
+__device__ __forceinline__ long long slice_start(long long i, long long T, long long G, bool small) {
+  return small ? (long long)((unsigned)T * (unsigned)i / (unsigned)G) : T * i / G;
+}
+// the slice containing position x (0 <= x < T)
+__device__ __forceinline__ long long owner_of(long long x, long long T, long long G, bool small) {
+  return small ? (long long)(((unsigned)x + 1u) * (unsigned)G - 1u) / (unsigned)T : ((x + 1) * G - 1) / T;
+}
+
+// Barrier among `threads` threads (whole warps) that all execute it with the
+// same id; id 0 is the one __syncthreads uses.
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 struct UnitSlices {
   long long first, last, us, n, T, G;
+  bool small;  // line_small(T, G)
   __device__ __forceinline__ bool has_part(long long i) const {
-    const long long a = T * i / G, z = T * (i + 1) / G;
+    const long long a = slice_start(i, T, G, small), z = slice_start(i + 1, T, G, small);
     return (a > us ? a : us) < (z < us + n ? z : us + n);
   }
   __device__ __forceinline__ int count() const {
@@ -279,10 +304,6 @@ __device__ __forceinline__ int unit_lag0(const DecodeParams& p, int v) {
   return MQ ? p.n_q - 1 - (v % p.n_cg) * p.tpg : 0;
 }
 
-// first / last thread block whose slice contains flattened page x
-__device__ __forceinline__ long long owner_of(long long x, long long T, long long G) {
-  return ((x + 1) * G - 1) / T;
-}
 
 // Block-wide inclusive scan of one int per thread (all threads call).
 __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total) {
@@ -1616,13 +1637,14 @@ template <int D, int G, int W, int SWZ, bool ROWS = false>
 __device__ __noinline__ void merge_stash_warp(const float* __restrict__ st_acc,
                                               const float* __restrict__ st_ml, int g,
                                               float* __restrict__ o_dst, float* __restrict__ lse_dst,
-                                              int gh = 1, int run = 0) {
+                                              int gh = 1, int run = 0, int hbeg = 0, int hstep = 1) {
   constexpr int CPL = D / 32;
   static_assert(CPL == 2 || CPL == 4, "head_dim 64 or 128");
   static_assert(SWZ < 2 || CPL == 4, "swizzles of bits 0-2 need four channels per lane");
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
+    if (hstep > 1 && h % hstep != hbeg) continue;  // heads hbeg, hbeg + hstep, ... only
     float mw[W];
     float M = -INFINITY;
 #pragma unroll
@@ -1723,6 +1745,19 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   pdl_launch_dependents();
   // the TMA descriptor is fetched while the plan runs
   if (tid == 0 && p.maps.valid) prefetch_tensormap(&p.maps.rec);
+  // the block table -> L2, each thread block a share of it, so that the
+  // staging of its entries below (after the plan) finds them there. Whole
+  // 16-byte words inside the table only. A prefetch is a hint: it is safe
+  // before the wait on the preceding kernel whatever that kernel writes.
+  if (tid == 32 && p.batch > 0) {
+    const int rows = MQ ? p.batch / p.n_cg : p.batch;  // real sequences (table rows)
+    const unsigned long long bytes = (unsigned long long)rows * (unsigned long long)p.max_blocks * 4ull;
+    const unsigned long long base = reinterpret_cast<unsigned long long>(p.block_table);
+    unsigned long long a = (base + bytes * (unsigned long long)cta / (unsigned long long)Gc + 15ull) & ~15ull;
+    const unsigned long long e = (base + bytes * (unsigned long long)(cta + 1) / (unsigned long long)Gc) & ~15ull;
+    for (; a < e; a += 32768ull)
+      prefetch_l2_bulk(reinterpret_cast<const void*>(a), (uint32_t)min(32768ull, e - a));
+  }
   bool waited = false;
   if (!p.early_plan) {
     pdl_wait();
@@ -1759,7 +1794,23 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   if (tid == 0) plan[0] = -1;
   int my_pages = 0, my_incl = 0;
   long long npages_all = 0;
-  {
+  if (p.batch <= 32) {
+    // at most 32 sequences: every warp loads and scans the lengths itself
+    // (the loads hit L1 after the first), so no block barrier is needed;
+    // warp 0's lanes hold the per-sequence values the one-pass plan uses
+    const int len = lane < p.batch ? vlen_checked<MQ>(p, lane, cta == 0 && warp == 0) : 0;
+    if (warp == 0 && lane < p.batch) lens_sm[lane] = len;
+    const int span = unit_span((len + BS - 1) / BS, p.unit_cost);
+    int x = span;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    my_incl = warp == 0 ? x : 0;
+    my_pages = warp == 0 ? span : 0;
+    npages_all = __shfl_sync(0xffffffffu, x, 31);
+  } else {
     int part = 0;
     for (int b = tid; b < p.batch; b += kThreads) {
       const int len = vlen_checked<MQ>(p, b, cta == 0);
@@ -1773,12 +1824,20 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   }
   // T: length of the cost line; this thread block's slice is [s_i, e_i)
   const long long T = npages_all * Hkv;
-  const long long s_i = T * cta / Gc, e_i = T * (cta + 1) / Gc;
+  const bool small = line_small(T, Gc);
+  const long long s_i = slice_start(cta, T, Gc, small), e_i = slice_start(cta + 1, T, Gc, small);
   // Ring stages in use (of the NST allocated): about one per 8 pages of a
   // slice, 16 to 24. Short slices run better with fewer pages in flight (the
   // first copies land sooner and HBM queues stay short); long ones need the
-  // depth. The same for every thread block of the launch.
-  const int nst = (int)max((long long)min(NST, kConsumerWarps), min((long long)NST, max(16LL, min(24LL, T / Gc / 8))));
+  // depth. The same for every thread block of the launch. A multiple of the
+  // consumer warp count, so that pages k and k + nst, which share a stage,
+  // belong to the same consumer warp: a warp then starts waiting for a fill
+  // only after it has itself released the fill before, and its parity wait
+  // can never mistake an older phase still in flight for the one it wants.
+  // (NST is a multiple of kConsumerWarps, so the result is at least one warp
+  // count.)
+  const int nst = (int)max((long long)min(NST, kConsumerWarps), min((long long)NST, max(16LL, min(24LL, (small ? (long long)((unsigned)T / (unsigned)Gc) : T / Gc) / 8)))) /
+                  kConsumerWarps * kConsumerWarps;
   // every thread block finds the sequence holding its first page
   if (one_pass) {
     const long long lo = (long long)(my_incl - my_pages) * Hkv, hi = (long long)my_incl * Hkv;
@@ -1897,8 +1956,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           const int sn = __shfl_sync(0xffffffffu, n, src);
           const int scn = __shfl_sync(0xffffffffu, cn, src);
           const int slen = __shfl_sync(0xffffffffu, len, src);
-          const int h_lo = (int)max(0LL, (wpos - sbase) / scn);
-          const int h_hi = (int)min((long long)Hkv - 1, (wlim - 1 - sbase) / scn);
+          // (both offsets below T; sbase < wlim)
+          const long long off_lo = wpos > sbase ? wpos - sbase : 0, off_hi = wlim - 1 - sbase;
+          const int h_lo = (int)(small ? (long long)((unsigned)off_lo / (unsigned)scn) : off_lo / scn);
+          const int h_hi = (int)min((long long)Hkv - 1,
+                                    small ? (long long)((unsigned)off_hi / (unsigned)scn) : off_hi / scn);
           for (int h = h_lo; h <= h_hi && !done; ++h) {
             // unit h: real pages [us, ure), then phantom positions up to ue
             const long long us = sbase + (long long)h * scn, ure = us + sn, ue = us + scn;
@@ -1915,7 +1977,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
                 sg.k0 = kcount;
                 sg.len = slen;
                 sg.us = us;
-                const long long first = owner_of(us, T, Gc), last = owner_of(ure - 1, T, Gc);
+                const long long first = owner_of(us, T, Gc, small), last = owner_of(ure - 1, T, Gc, small);
                 sg.slot = first == last ? -1 : (int)(cta + sb * Hkv + h);
                 // a unit's pages are contiguous within a slice: a run that starts
                 // after both the unit's and the slice's first page continues the
@@ -1970,6 +2032,19 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       // of up to kStageLoads * kThreads pages)
       constexpr int kStageLoads = 4;
       const int nwin = kw1 - kw0;
+      // the window's q rows -> L2 too (a hint, safe before the wait), so
+      // that the producer's copies of them land fast
+      if (warp == 0) {
+        for (int qi = lane; qi < nseg; qi += 32) {
+          if constexpr (MQ) {
+            for (int c = 0; c < unit_cols<MQ>(p, segs[qi].b); c += p.g_heads)
+              prefetch_l2_bulk(p.q + unit_row<MQ>(p, segs[qi].b, segs[qi].h, c) * D, p.g_heads * D * 2);
+          } else {
+            const uint16_t* qsrc = p.q + ((long long)segs[qi].b * p.num_q_heads + (long long)segs[qi].h * g) * D;
+            prefetch_l2_bulk(qsrc, g * D * 2);
+          }
+        }
+      }
       for (int i0 = 0; i0 < nwin; i0 += kStageLoads * kThreads) {
         int v[kStageLoads];
 #pragma unroll
@@ -1997,6 +2072,38 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     }
     __syncthreads();
     wait_and_publish();  // first window only: pages and outputs follow
+
+    // merge the stash of unit sg into its row or partial: heads hbeg,
+    // hbeg + hstep, ... (all of them with the defaults)
+    auto merge_unit = [&](const Seg& sg, int hbeg, int hstep) {
+      const long long row0 = (long long)sg.b * p.num_q_heads + (long long)sg.h * g;
+      if constexpr (MQ) {
+        // rows of the column group: g_heads per query token, a token's rows
+        // num_q_heads apart
+        const int cols = unit_cols<MQ>(p, sg.b);
+        if (sg.slot < 0)
+          merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz, true>(
+              stash_acc, stash_ml, cols, p.out + unit_row<MQ>(p, sg.b, sg.h, 0) * D, nullptr, p.g_heads,
+              p.num_q_heads, hbeg, hstep);
+        else
+          merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(
+              stash_acc, stash_ml, cols, p.part_o + (long long)sg.slot * g * D, p.part_lse + (long long)sg.slot * g,
+              1, 0, hbeg, hstep);
+      } else if (sg.slot < 0) {
+        merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.out + row0 * D, nullptr,
+                                                                1, 0, hbeg, hstep);
+      } else {
+        merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g,
+                                                                p.part_o + (long long)sg.slot * g * D,
+                                                                p.part_lse + (long long)sg.slot * g, 1, 0, hbeg, hstep);
+      }
+    };
+    // The slice's last unit: its merge ends this thread block's critical
+    // path, and the consumer warps have no pages left, so they share it with
+    // the merger warp (heads split over the kConsumerWarps + 1 warps), then
+    // meet at named barrier 1.
+    constexpr int kMergeWarps = kConsumerWarps + 1;
+    const int last_si = wend >= e_i ? nseg - 1 : -1;
 
     if (warp == 0) {
       // ---------------------------------------------------------- producer
@@ -2042,16 +2149,6 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         }
         return true;
       };
-      // the window's q rows -> L2 now, so that a q sent late still lands fast
-      for (int qi = lane; qi < nseg; qi += 32) {
-        if constexpr (MQ) {
-          for (int c = 0; c < unit_cols<MQ>(p, segs[qi].b); c += p.g_heads)
-            prefetch_l2_bulk(p.q + unit_row<MQ>(p, segs[qi].b, segs[qi].h, c) * D, p.g_heads * D * 2);
-        } else {
-          const uint16_t* qsrc = p.q + ((long long)segs[qi].b * p.num_q_heads + (long long)segs[qi].h * g) * D;
-          prefetch_l2_bulk(qsrc, g * D * 2);
-        }
-      }
       int qseg = 0;    // segments whose first page the issue has reached
       int q_sent = 0;  // segments whose q has been sent (lane 0's count)
       for (int k = kw0; k < kw1;) {
@@ -2176,6 +2273,16 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         cons.deposit(stash_acc + cw * G * D, stash_ml + cw * G * 2);
         __syncwarp();
         if (lane == 0) mbar_arrive(deposited);  // release: the stash rows above
+        if (si == last_si) {
+          const bool okd = mbar_wait_bounded(deposited, (n_dep - 1) & 1);  // every warp's state is in
+          if (!okd && abort_flag == 0) {
+            if (lane == 0) set_error(p.pool.err, PA_DEVERR_TIMEOUT);
+            abort_flag = 1;
+          }
+          merge_unit(sg, cw, kMergeWarps);
+          if (p.fused) __threadfence();  // this warp's partial rows before the merger's ticket
+          named_bar_sync(1, kMergeWarps * 32);
+        }
       }
     } else {
       // ---------------------------------------------------------- merger
@@ -2196,23 +2303,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         }
         ++n_dep;
         const long long row0 = (long long)sg.b * p.num_q_heads + (long long)sg.h * g;
-        if constexpr (MQ) {
-          // rows of the column group: g_heads per query token, a token's rows
-          // num_q_heads apart
-          const int cols = unit_cols<MQ>(p, sg.b);
-          if (sg.slot < 0)
-            merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz, true>(
-                stash_acc, stash_ml, cols, p.out + unit_row<MQ>(p, sg.b, sg.h, 0) * D, nullptr, p.g_heads,
-                p.num_q_heads);
-          else
-            merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, cols,
-                                                                    p.part_o + (long long)sg.slot * g * D,
-                                                                    p.part_lse + (long long)sg.slot * g);
-        } else if (sg.slot < 0) {
-          merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.out + row0 * D, nullptr);
+        if (si == last_si) {
+          merge_unit(sg, kConsumerWarps, kMergeWarps);
+          named_bar_sync(1, kMergeWarps * 32);
         } else {
-          merge_stash_warp<D, G, kConsumerWarps, Cons::kStashSwz>(stash_acc, stash_ml, g, p.part_o + (long long)sg.slot * g * D,
-                                                                  p.part_lse + (long long)sg.slot * g);
+          merge_unit(sg, 0, 1);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(merged);  // the stash may be overwritten
@@ -2226,8 +2321,9 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           usl.us = sg.us;
           usl.T = T;
           usl.G = Gc;
-          usl.first = owner_of(usl.us, T, Gc);
-          usl.last = owner_of(usl.us + usl.n - 1, T, Gc);
+          usl.small = small;
+          usl.first = owner_of(usl.us, T, Gc, small);
+          usl.last = owner_of(usl.us + usl.n - 1, T, Gc, small);
           const long long u = (long long)sg.b * Hkv + sg.h;
           int last_slice = 0;
           if (lane == 0) {
@@ -2283,8 +2379,14 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
 // With MQ (several query tokens per sequence) the units are those of the
 // virtual sequences (see DecodeParams): lengths come from sequence b / n_cg
 // and column c of a unit goes to its own row.
+// Four warps (one per SM sub-partition) and at most 112 registers a thread:
+// small enough to share an SM with a decode thread block, whose two warps on
+// one sub-partition take 12.8 K of its 16 K registers, so the combine of one
+// call and the decode of the next can both be resident. Launched with
+// kCombineThreads threads.
+constexpr int kCombineThreads = 128;
 template <int D, bool MQ = false>
-__global__ void __launch_bounds__(256)
+__global__ void __maxnreg__(112)
     splitkv_combine_kernel(const int32_t* seq_lens, const int32_t* pre_cost, const float* part_o,
                            const float* part_lse, float* out, int batch, int num_kv_heads, int group,
                            int num_q_heads, int num_ctas, int block_size, int max_blocks, int unit_cost,
@@ -2348,8 +2450,9 @@ __global__ void __launch_bounds__(256)
     usl.n = n;
     usl.T = T;
     usl.G = num_ctas;
-    usl.first = n > 0 ? owner_of(usl.us, T, num_ctas) : 0;
-    usl.last = n > 0 ? owner_of(usl.us + n - 1, T, num_ctas) : 0;
+    usl.small = line_small(T, num_ctas);
+    usl.first = n > 0 ? owner_of(usl.us, T, num_ctas, usl.small) : 0;
+    usl.last = n > 0 ? owner_of(usl.us + n - 1, T, num_ctas, usl.small) : 0;
     const int cnt = (int)min((long long)kMaxSl, usl.last - usl.first + 1);
     for (int i = 0; i < cnt && usl.first != usl.last; ++i)
       if (usl.has_part(usl.first + i)) mask0 |= 1ull << i;
@@ -2382,11 +2485,24 @@ __global__ void __launch_bounds__(256)
     return;
   }
   if (usl.first == usl.last) return;
-  // this thread's four channels of head h
-  const int e0 = tid * 4;
-  if (e0 >= cols * D) return;
-  const int h = e0 / D;
-  float M = -INFINITY, W = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // this thread's quads: four channels of one column each, quads tid and
+  // tid + 128 of the unit's cols * D / 4 (at most 256: 8 columns of 128)
+  constexpr int kQ = 2;
+  const int nquad = cols * D / 4;
+  if (tid >= nquad) return;
+  int e0[kQ], hq[kQ];
+  bool act[kQ];
+  float M[kQ], W[kQ], A[kQ][4];
+#pragma unroll
+  for (int x = 0; x < kQ; ++x) {
+    const int qd = tid + x * kCombineThreads;
+    act[x] = qd < nquad;
+    e0[x] = act[x] ? qd * 4 : 0;
+    hq[x] = e0[x] / D;
+    M[x] = -INFINITY;
+    W[x] = 0.0f;
+    A[x][0] = A[x][1] = A[x][2] = A[x][3] = 0.0f;
+  }
   for (long long s0 = usl.first; s0 <= usl.last; s0 += kMaxSl) {
     const int cnt = (int)min((long long)kMaxSl, usl.last - s0 + 1);
     // slices of this round holding a partial (block-uniform)
@@ -2396,39 +2512,50 @@ __global__ void __launch_bounds__(256)
       for (int i = 0; i < cnt; ++i)
         if (usl.has_part(s0 + i)) mask |= 1ull << i;
     }
-    // one round of loads: lse and four channels of every partial
-    constexpr int kBatch = 8;
+    // one round of loads: lse and the quads of kBatch partials
+    constexpr int kBatch = 4;
     for (int i0 = 0; i0 < cnt; i0 += kBatch) {
-      float l[kBatch];
-      float4 o[kBatch];
+      float l[kQ][kBatch];
+      float4 o[kQ][kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int i = i0 + k;
-        l[k] = -INFINITY;
-        o[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (i < cnt && ((mask >> i) & 1)) {
-          const long long slot = s0 + i + u;
-          l[k] = __ldcg(part_lse + slot * group + h);
-          o[k] = __ldcg(reinterpret_cast<const float4*>(part_o + slot * group * D + e0));
+        const bool has = i < cnt && ((mask >> i) & 1);
+        const long long slot = s0 + i + u;
+#pragma unroll
+        for (int x = 0; x < kQ; ++x) {
+          l[x][k] = -INFINITY;
+          o[x][k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (has && act[x]) {
+            l[x][k] = __ldcg(part_lse + slot * group + hq[x]);
+            o[x][k] = __ldcg(reinterpret_cast<const float4*>(part_o + slot * group * D + e0[x]));
+          }
         }
       }
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (l[k] == -INFINITY) continue;
-        const float Mn = fmaxf(M, l[k]);
-        const float a = M == -INFINITY ? 0.0f : exp2f(M - Mn), w = exp2f(l[k] - Mn);
-        W = W * a + w;
-        A[0] = A[0] * a + w * o[k].x;
-        A[1] = A[1] * a + w * o[k].y;
-        A[2] = A[2] * a + w * o[k].z;
-        A[3] = A[3] * a + w * o[k].w;
-        M = Mn;
-      }
+      for (int x = 0; x < kQ; ++x)
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (l[x][k] == -INFINITY) continue;
+          const float Mn = fmaxf(M[x], l[x][k]);
+          const float a = M[x] == -INFINITY ? 0.0f : exp2f(M[x] - Mn), w = exp2f(l[x][k] - Mn);
+          W[x] = W[x] * a + w;
+          A[x][0] = A[x][0] * a + w * o[x][k].x;
+          A[x][1] = A[x][1] * a + w * o[x][k].y;
+          A[x][2] = A[x][2] * a + w * o[x][k].z;
+          A[x][3] = A[x][3] * a + w * o[x][k].w;
+          M[x] = Mn;
+        }
     }
   }
-  const float inv = W > 0.0f ? 1.0f / W : 0.0f;
-  float* dst = MQ ? out + out_row(h) * D + (e0 - h * D) : out + row0 * D + e0;
-  *reinterpret_cast<float4*>(dst) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
+#pragma unroll
+  for (int x = 0; x < kQ; ++x) {
+    if (!act[x]) continue;
+    const float inv = W[x] > 0.0f ? 1.0f / W[x] : 0.0f;
+    const int h = hq[x];
+    float* dst = MQ ? out + out_row(h) * D + (e0[x] - h * D) : out + row0 * D + e0[x];
+    *reinterpret_cast<float4*>(dst) = make_float4(A[x][0] * inv, A[x][1] * inv, A[x][2] * inv, A[x][3] * inv);
+  }
 }
 
 template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ = false>
@@ -2455,7 +2582,7 @@ cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_
   const int units = prm.batch * prm.pool.num_kv_heads;
   if (units == 0 || prm.fused) return cudaSuccess;
   cfg.gridDim = dim3(units);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<D, MQ>, prm.seq_lens, (const int32_t*)prm.pre_cost,
                             (const float*)prm.part_o, (const float*)prm.part_lse, prm.out, prm.batch,
