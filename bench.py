@@ -2,23 +2,38 @@
 step's new token of every sequence (kv_quant_append), then attend
 (paged_gqa_decode + split-KV combine) -- on the Qwen2.5-7B-shaped workload
 (batch 32, 28 Q / 4 KV heads, head_dim 128, block 16, seq_lens U[512, 4096],
-bf16 KV), synthetic seeded data.
+bf16 KV), synthetic seeded data. The same run measures the other workloads
+(Qwen3-8B-shaped uint8 and fp8 KV, long-context uint4, prefix-sharing mix)
+under "per_config".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--splits S]
+                  [--workload NAME] [--splits S] [--no-per-config]
 
 Prints one JSON line. value = decode tokens per second (batch / step time),
-whole job over all ranks. The L2 cache is flushed (a 256 MiB write) between
-timed steps, outside the per-step CUDA-event brackets. Under torchrun every
-rank runs its own replica of the workload (the path needs no exchange between
-GPUs): weak scaling.
+whole job over all ranks. Two timings of each workload:
+  isolated      every step (and every decode call) bracketed by its own CUDA
+                events, with the L2 cache flushed (a 256 MiB write) before it,
+                outside the brackets; `value`, `ms_per_step` and `roofline`
+                come from these;
+  back_to_back  K steps (calls) in one pair of events, each reading another
+                of several copies of the pool (every copy larger than L2), as
+                a decoding loop issues them.
+`stream_ceiling` times a plain read of the same number of bytes both ways: it
+is what the launch, ramp-up and drain of one kernel cost at this size.
+
+With --gpus N > 1 and no torchrun environment the script starts N local
+ranks itself (torch.distributed.run, 127.0.0.1). Every rank runs its own
+replica of the workload on its own GPU (the path needs no exchange between
+GPUs): weak scaling; times are the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import platform
 import re
+import socket
 import statistics
 import subprocess
 import sys
@@ -43,11 +58,25 @@ WORKLOAD_TEXT = {
                   "block 16, lognormal(median 1000) lengths, 8x32 sequences share 512-token prefixes, bf16 KV",
     "tiny": "tiny: batch 2, 4 Q / 2 KV heads, head_dim 64, block 16, seq_lens {37,5}, bf16 KV",
 }
+# measured in the same run as the headline workload
+PER_CONFIG = ("qwen3_8b_int8", "long_uint4", "prefix_mix", "qwen3_8b_fp8")
+L2_BYTES = 129 * 1000 * 1000
+L2_TEXT = ("GPU arm, isolated: L2 flushed before every timed step and call (a 256 MiB write, outside the event "
+           "brackets); GPU arm, back_to_back: inputs larger than L2 (each call reads another of {n} pool copies "
+           "of {mb:.0f} MB); CPU arm: host memory")
+
+
+def pool_copies(nbytes):
+    """Pool copies the back-to-back timing rotates through: enough that every
+    call reads memory that the calls before it pushed out of L2."""
+    return max(2, -(-3 * L2_BYTES // max(int(nbytes), 1)))
 
 
 PROFILE_FOR = {"qwen25_7b_bf16": "profiles/paged_gqa_decode_qwen25_7b_bf16.md",
                "qwen3_8b_int8": "profiles/paged_gqa_decode_qwen3_8b_int8.md",
-               "long_uint4": "profiles/paged_gqa_decode_long_uint4.md"}
+               "long_uint4": "profiles/paged_gqa_decode_long_uint4.md",
+               "prefix_mix": "profiles/paged_gqa_decode_prefix_mix.md",
+               "qwen3_8b_fp8": "profiles/paged_gqa_decode_qwen3_8b_fp8.md"}
 
 
 # The consumer sections of the decode source each workload's tensor-core
@@ -111,6 +140,17 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 class ClockSampler:
@@ -187,12 +227,236 @@ def _barrier(dist):
         dist.barrier()
 
 
+def workload_config(wl, name, n_q, world=1):
+    """The workload's description, the same for both arms of the benchmark."""
+    from paged_gqa_decode_02_gb300.metrics import decode_bytes
+    nb = decode_bytes(wl, n_q)
+    cfg = {"workload": WORKLOAD_TEXT[name], "name": name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+           "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+           "kv_dtype": wl.kv_dtype, "tokens_cached": nb["tokens_scanned"], "query_tokens": n_q,
+           "step": (f"append {n_q} token(s)/seq (kv_quant_append) + paged_gqa_decode"
+                    + (f" with {n_q} causal query tokens per sequence" if n_q > 1 else "")
+                    + " + split-KV combine"),
+           "l2": L2_TEXT.format(n=pool_copies(nb["algorithmic"]), mb=nb["algorithmic"] / 1e6),
+           "parallelism": f"replicas x{world} (no exchange)"}
+    return cfg, nb
+
+
+class WorkloadRun:
+    """One workload on one GPU: `n_rot` identical pools (the copies that the
+    back-to-back timing rotates through), the step's inputs, and timers."""
+
+    def __init__(self, name, args, dev, n_q=1, n_rot=None):
+        import torch
+        from paged_gqa_decode_02_gb300 import workloads as W
+        from paged_gqa_decode_02_gb300.binding import PagedKVPool
+        self.torch = torch
+        self.name, self.args, self.dev, self.n_q = name, args, dev, n_q
+        wl = self.wl = W.CONFIGS[name]()
+        self.cfg, self.nb = workload_config(wl, name, n_q, int(os.environ.get("WORLD_SIZE", "1")))
+        self.n_rot = n_rot or pool_copies(self.nb["algorithmic"])
+        fills = [(self.d(c.k_bits), self.d(c.v_bits), self.d(c.cu_new), self.d(c.ctx_lens),
+                  self.d(c.block_table), c.max_new) for c in wl.fill_calls(leave_last=(n_q == 1))]
+        self.pools = []
+        for _ in range(self.n_rot):
+            p = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, dev.index)
+            p.set_decode_path(args.path, fused_combine=(args.combine == "fused"), early_plan=not args.no_early_plan)
+            p.set_unit_cost(args.unit_cost)
+            for k, v, cu, ctx, tb, mn in fills:
+                p.append_kv(k, v, cu, ctx, tb, max_new_per_seq=mn)
+            self.pools.append(p)
+        del fills
+        step = self.step = wl.step_call(n_q)
+        self.st = (self.d(step.k_bits), self.d(step.v_bits), self.d(step.cu_new), self.d(step.ctx_lens))
+        B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
+        self.q_bits = wl.q_bits if n_q == 1 else W.multi_token_queries(100, B, n_q, Hq, D)
+        self.table, self.lens, self.q = self.d(wl.block_table), self.d(wl.seq_lens), self.d(self.q_bits)
+        self.outs = [torch.empty(self.q_bits.shape, dtype=torch.float32, device=dev) for _ in range(self.n_rot)]
+        self.ws = [p.workspace(B, Hq, args.splits) for p in self.pools]
+        self.splits_used = self.pools[0].num_splits(args.splits)
+        self.flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def d(self, a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return self.torch.from_numpy(a).to(self.dev)
+
+    def decode_call(self, i, q=None, table=None, lens=None):
+        q = self.q if q is None else q
+        table = self.table if table is None else table
+        lens = self.lens if lens is None else lens
+        p, out = self.pools[i], self.outs[i]
+        if self.n_q == 1:
+            p.decode(q, table, lens, self.wl.softmax_scale, out=out, workspace=self.ws[i],
+                     num_splits=self.args.splits)
+        else:
+            p.decode_multi(q, table, lens, self.wl.softmax_scale, out=out, num_splits=self.args.splits)
+
+    def step_call(self, i):
+        # append then decode back to back, as a decode loop runs them (the
+        # decode's planning may overlap the append; see --no-early-plan)
+        k, v, cu, ctx = self.st
+        self.pools[i].append_kv(k, v, cu, ctx, self.table, max_new_per_seq=self.n_q)
+        self.decode_call(i)
+
+    def isolated(self, fn, K):
+        torch = self.torch
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            self.flush.fill_(1)
+            e0[i].record(self.stream)
+            fn(0)
+            e1[i].record(self.stream)
+        torch.cuda.synchronize()
+        return [e0[i].elapsed_time(e1[i]) for i in range(K)]
+
+    def back_to_back(self, fn, K):
+        torch = self.torch
+        for i in range(self.n_rot):
+            fn(i)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        for i in range(K):
+            fn(i % self.n_rot)
+        z.record(self.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) / K
+
+    def e2e(self, K):
+        """The step through the public API from pinned host buffers: H2D of the
+        step's inputs, append, decode, D2H of the output, all in the region."""
+        torch = self.torch
+        s = self.step
+        h_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else
+                                    np.ascontiguousarray(v)).pin_memory()
+                for k, v in (("k", s.k_bits), ("v", s.v_bits), ("cu", s.cu_new), ("ctx", s.ctx_lens),
+                             ("table", self.wl.block_table), ("lens", self.wl.seq_lens), ("q", self.q_bits))}
+        h_out = torch.empty(self.q_bits.shape, dtype=torch.float32).pin_memory()
+        d_in = {k: torch.empty_like(v, device=self.dev) for k, v in h_in.items()}
+        bi = sum(v.numel() * v.element_size() for v in h_in.values())
+        bo = h_out.numel() * h_out.element_size()
+        ms = []
+        for i in range(K + 3):
+            self.flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            for k in d_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+            self.pools[0].append_kv(d_in["k"], d_in["v"], d_in["cu"], d_in["ctx"], d_in["table"],
+                                    max_new_per_seq=self.n_q)
+            self.decode_call(0, d_in["q"], d_in["table"], d_in["lens"])
+            h_out.copy_(self.outs[0], non_blocking=True)
+            z.record(self.stream)
+            z.synchronize()
+            if i >= 3:
+                ms.append(a.elapsed_time(z))
+        return statistics.mean(ms), bi, bo
+
+    def device_error(self):
+        for p in self.pools:
+            st, flags = p.device_error()
+            if st != 0 or flags != 0:
+                return st, flags
+        return 0, 0
+
+    def close(self):
+        for p in self.pools:
+            p.close()
+        self.pools = []
+
+
+def measure(run, dist, world, K, warmup, peak, peak_kind, K_e2e):
+    """All timings of one workload (max over ranks); the JSON fields."""
+    B, n_q = run.wl.batch, run.n_q
+    for _ in range(max(3, warmup)):
+        run.flush.fill_(1)
+        run.step_call(0)
+    run.torch.cuda.synchronize()
+    st, flags = run.device_error()
+    assert st == 0 and flags == 0, f"device error word {flags:#x} during warm-up ({run.name})"
+    _barrier(dist)
+    step_ms = run.isolated(run.step_call, K)
+    dec_ms = run.isolated(run.decode_call, K)
+    b2b_step = run.back_to_back(run.step_call, K)
+    b2b_dec = run.back_to_back(run.decode_call, K)
+    st, flags = run.device_error()
+    assert st == 0 and flags == 0, f"device error word {flags:#x} during timing ({run.name})"
+    t_step = _max_over_ranks(dist, statistics.mean(step_ms) / 1e3)
+    t_dec = _max_over_ranks(dist, statistics.mean(dec_ms) / 1e3)
+    t_b2b_step = _max_over_ranks(dist, b2b_step / 1e3)
+    t_b2b_dec = _max_over_ranks(dist, b2b_dec / 1e3)
+    e2e_ms, bi, bo = run.e2e(K_e2e)
+    t_e2e = _max_over_ranks(dist, e2e_ms / 1e3)
+    alg = run.nb["algorithmic"]
+    ach = alg / t_dec / 1e9
+    ach_b2b = alg / t_b2b_dec / 1e9
+    return {
+        "value": world * B * n_q / t_step,
+        "ms_per_step": t_step * 1e3,
+        "decode_us": t_dec * 1e6,
+        "median_us": {"step": statistics.median(step_ms) * 1e3, "decode": statistics.median(dec_ms) * 1e3},
+        "hbm_gbs": ach,
+        "kv_tokens_per_s": world * run.nb["tokens_scanned"] / t_dec,
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                     "traffic": _traffic(run.name, run.args.path) if n_q == 1 else None,
+                     "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg,
+                     "timed": "pa_decode call (decode kernel + split-KV combine) alone, isolated: CUDA events "
+                              "on the launch stream around each call, L2 flushed before it"},
+        "back_to_back": {"step_us": t_b2b_step * 1e6, "decode_us": t_b2b_dec * 1e6,
+                         "tokens_per_s": world * B * n_q / t_b2b_step,
+                         "decode_gbs": ach_b2b, "decode_frac": ach_b2b / peak, "pool_copies": run.n_rot},
+        "e2e": {"value": world * B * n_q / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "launch": {"num_splits": run.splits_used, "decode_path": run.args.path,
+                   "combine": run.args.combine if n_q == 1 else "separate", "early_plan": not run.args.no_early_plan,
+                   "unit_cost": run.args.unit_cost},
+    }
+
+
+def stream_ceiling(dev, nbytes, K):
+    """A plain read of `nbytes` (torch's sum over a float32 buffer), timed like
+    the decode call: isolated with the L2 flushed, and back to back over three
+    copies. What one kernel's launch, ramp-up and drain cost at this size."""
+    import torch
+    n = max(1, nbytes // 4)
+    bufs = [torch.ones(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for b in bufs:
+        b.sum()
+    ms = []
+    for i in range(K):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record()
+        bufs[0].sum()
+        z.record()
+        ms.append((a, z))
+    torch.cuda.synchronize()
+    iso = statistics.mean(a.elapsed_time(z) for a, z in ms) / 1e3
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        bufs[i % 3].sum()
+    z.record()
+    torch.cuda.synchronize()
+    b2b = a.elapsed_time(z) / K / 1e3
+    return {"bytes": n * 4, "isolated_us": iso * 1e6, "isolated_gbs": n * 4 / iso / 1e9,
+            "back_to_back_us": b2b * 1e6, "back_to_back_gbs": n * 4 / b2b / 1e9,
+            "kernel": "torch.sum over a float32 buffer (a read of the same bytes)"}
+
+
 def run_ours(args):
     import torch
     from paged_gqa_decode_02_gb300 import build as pbuild
-    from paged_gqa_decode_02_gb300 import workloads as W
-    from paged_gqa_decode_02_gb300.binding import PagedKVPool
-    from paged_gqa_decode_02_gb300.metrics import decode_bytes
 
     dist, rank, world = _dist()
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -200,174 +464,96 @@ def run_ours(args):
     if rank == 0:
         pbuild.build()
     _barrier(dist)
-    wl = W.CONFIGS[args.workload]()
     dev = torch.device("cuda", local)
-    pool = PagedKVPool(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, wl.kv_dtype, local)
-    pool.set_decode_path(args.path, fused_combine=(args.combine == "fused"),
-                         early_plan=not args.no_early_plan)
-    pool.set_unit_cost(args.unit_cost)
-
-    def d(a):
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint16:
-            a = a.view(np.int16)
-        return torch.from_numpy(a).to(dev)
-
-    # several query tokens per sequence (chunked prefill / speculative
-    # verification): the step appends the last n_q tokens and attends with all
+    peak, peak_kind = _peaks()
+    K = args.steps
     n_q = args.query_tokens
-    for c in wl.fill_calls(leave_last=(n_q == 1)):
-        pool.append_kv(d(c.k_bits), d(c.v_bits), d(c.cu_new), d(c.ctx_lens), d(c.block_table),
-                       max_new_per_seq=c.max_new)
-    step = wl.step_call(n_q)
-    st_k, st_v, st_cu, st_ctx = d(step.k_bits), d(step.v_bits), d(step.cu_new), d(step.ctx_lens)
-    B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
-    q_bits = wl.q_bits if n_q == 1 else W.multi_token_queries(100, B, n_q, Hq, D)
-    table, seq_lens, q = d(wl.block_table), d(wl.seq_lens), d(q_bits)
-    out = torch.empty(q_bits.shape, dtype=torch.float32, device=dev)
-    ws = pool.workspace(B, Hq, args.splits)
-    splits_used = pool.num_splits(args.splits)
 
-    def decode_call(q_, table_, lens_):
-        if n_q == 1:
-            pool.decode(q_, table_, lens_, wl.softmax_scale, out=out, workspace=ws, num_splits=args.splits)
-        else:
-            pool.decode_multi(q_, table_, lens_, wl.softmax_scale, out=out, num_splits=args.splits)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def one_step():
-        # append then decode back to back, as a decode loop runs them (the
-        # decode's planning may overlap the append; see --no-early-plan)
-        pool.append_kv(st_k, st_v, st_cu, st_ctx, table, max_new_per_seq=n_q)
-        decode_call(q, table, seq_lens)
-
-    for _ in range(max(3, args.warmup)):
-        flush.fill_(1)
-        one_step()
-    torch.cuda.synchronize()
-    st, flags = pool.device_error()
-    assert st == 0 and flags == 0, f"device error word {flags:#x} during warm-up"
-
+    run = WorkloadRun(args.workload, args, dev, n_q)
     clocks = ClockSampler(local)
     clocks.start()
     # soak so that the clock record covers a loaded GPU before and during timing
     t_end = time.time() + 1.0
     while time.time() < t_end:
-        flush.fill_(1)
-        one_step()
+        run.flush.fill_(1)
+        run.step_call(0)
     torch.cuda.synchronize()
-
-    K = args.steps
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    _barrier(dist)
-    torch.cuda.synchronize()
-    for i in range(K):
-        flush.fill_(1)
-        e0[i].record(stream)
-        one_step()
-        e2[i].record(stream)
-    torch.cuda.synchronize()
-    _barrier(dist)
-    # roofline of the decode call alone: a second pass of K calls, each
-    # bracketed by events (L2 flushed before each)
-    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        flush.fill_(1)
-        d0[i].record(stream)
-        decode_call(q, table, seq_lens)
-        d1[i].record(stream)
-    torch.cuda.synchronize()
+    head = measure(run, dist, world, K, args.warmup, peak, peak_kind, max(10, min(K, 200)))
+    ceiling = stream_ceiling(dev, run.nb["algorithmic"], min(K, 500))
     clk = clocks.stop()
-    step_ms = [e0[i].elapsed_time(e2[i]) for i in range(K)]
-    dec_ms = [d0[i].elapsed_time(d1[i]) for i in range(K)]
-    st, flags = pool.device_error()
-    assert st == 0 and flags == 0, f"device error word {flags:#x} during timing"
-    t_step = statistics.mean(step_ms) / 1e3
-    t_dec = statistics.mean(dec_ms) / 1e3
-    t_step_max = _max_over_ranks(dist, t_step)
-    t_dec_max = _max_over_ranks(dist, t_dec)
-
-    # ---- e2e through the public API with host buffers (pinned), copies inside the region
-    h_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else
-                                np.ascontiguousarray(v)).pin_memory()
-            for k, v in (("k", step.k_bits), ("v", step.v_bits), ("cu", step.cu_new), ("ctx", step.ctx_lens),
-                         ("table", wl.block_table), ("lens", wl.seq_lens), ("q", q_bits))}
-    h_out = torch.empty(q_bits.shape, dtype=torch.float32).pin_memory()
-    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
-    bi = sum(v.numel() * v.element_size() for v in h_in.values())
-    bo = h_out.numel() * h_out.element_size()
-    Ke = max(10, min(K, 200))
-    e2e_ms = []
-    for i in range(Ke + 3):
-        flush.fill_(1)
-        a = torch.cuda.Event(enable_timing=True)
-        z = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for k in d_in:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        pool.append_kv(d_in["k"], d_in["v"], d_in["cu"], d_in["ctx"], d_in["table"], max_new_per_seq=n_q)
-        decode_call(d_in["q"], d_in["table"], d_in["lens"])
-        h_out.copy_(out, non_blocking=True)
-        z.record(stream)
-        z.synchronize()
-        if i >= 3:
-            e2e_ms.append(a.elapsed_time(z))
-    t_e2e = _max_over_ranks(dist, statistics.mean(e2e_ms) / 1e3)
-
-    nb = decode_bytes(wl, n_q)
-    peak, peak_kind = _peaks()
-    achieved = nb["algorithmic"] / t_dec_max / 1e9
+    cfg = dict(run.cfg)
     res = {
         "metric": METRIC,
-        "value": world * B * n_q / t_step_max,
+        "value": head["value"],
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": t_step_max * 1e3,
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if wl.kv_dtype == "bf16" else f"{wl.kv_dtype} codes, fp32 math",
+        "dtype": "bf16" if run.wl.kv_dtype == "bf16" else f"{run.wl.kv_dtype} codes, fp32 math",
         "data": "synthetic (seeded N(0,1) bf16 q/K/V, block tables from a seeded permutation)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": B,
-                   "num_q_heads": Hq, "num_kv_heads": wl.num_kv_heads, "head_dim": D,
-                   "block_size": wl.block_size, "kv_dtype": wl.kv_dtype,
-                   "tokens_cached": nb["tokens_scanned"], "num_splits": splits_used,
-                   "step": (f"append {n_q} token(s)/seq (kv_quant_append) + paged_gqa_decode"
-                            + (f" with {n_q} causal query tokens per sequence" if n_q > 1 else "")
-                            + " (split-KV merge: " + (args.combine if n_q == 1 else "separate") + ")"),
-                   "query_tokens": n_q,
-                   "decode_path": args.path,
-                   "early_plan": not args.no_early_plan,
-                   "unit_cost": args.unit_cost,
-                   "l2": "flushed before every timed step (256 MiB write, outside the event brackets)",
-                   "parallelism": f"replicas x{world} (no exchange)"},
-        "hbm_gbs": achieved,
-        "decode_us": t_dec_max * 1e6,
-        "median_us": {"step": statistics.median(step_ms) * 1e3, "decode": statistics.median(dec_ms) * 1e3},
-        "kv_tokens_per_s": world * nb["tokens_scanned"] / t_dec_max,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     "traffic": _traffic(args.workload, args.path) if n_q == 1 else None,
-                     "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": nb["algorithmic"],
-                     "timed": "pa_decode call (decode kernel + split-KV combine) alone, CUDA events on the "
-                              "launch stream, a second pass of K calls after the K timed steps"},
-        "e2e": {"value": world * B * n_q / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
-        "gpu_launches": 3 * K,
-        "clocks": clk,
+        "config": cfg,
     }
+    res.update({k: v for k, v in head.items() if k not in ("value", "ms_per_step")})
+    res["stream_ceiling"] = ceiling
+    res["gpu_launches"] = 3 * K
+    res["gpu_launches_note"] = "3 per step in the isolated step timing: kv_append_kernel, " \
+                               "paged_gqa_decode_kernel, splitkv_combine_kernel"
+    res["clocks"] = clk
+    run.close()
+    del run
+    torch.cuda.empty_cache()
+
+    if not args.no_per_config and n_q == 1:
+        per = {}
+        Kp = max(3, min(K, 300))
+        pclk = ClockSampler(local)
+        pclk.start()
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            r = WorkloadRun(name, args, dev, 1)
+            m = measure(r, dist, world, Kp, args.warmup, peak, peak_kind, max(10, min(Kp, 100)))
+            m["config"] = dict(r.cfg)
+            m["steps"] = Kp
+            m["dtype"] = "bf16" if r.wl.kv_dtype == "bf16" else f"{r.wl.kv_dtype} codes, fp32 math"
+            if name == "prefix_mix":
+                m["logical_bytes"] = r.nb["logical"]
+                m["effective_gbs"] = r.nb["logical"] / (m["decode_us"] / 1e6) / 1e9
+            per[name] = m
+            r.close()
+            del r
+            torch.cuda.empty_cache()
+        res["per_config"] = per
+        res["per_config_clocks"] = pclk.stop()
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seqs, n_q)
+        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seqs, n_q)
     if rank == 0:
         print(json.dumps(res), flush=True)
-    pool.close()
+
+
+def profile_run(args):
+    """W warm-up steps, then K isolated steps of one pool: per step the L2
+    flush (torch fill), kv_append_kernel, paged_gqa_decode_kernel and
+    splitkv_combine_kernel, and nothing else."""
+    import torch
+    from paged_gqa_decode_02_gb300 import build as pbuild
+    pbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    run = WorkloadRun(args.workload, args, dev, args.query_tokens, n_rot=1)
+    for _ in range(max(3, args.warmup)):
+        run.flush.fill_(1)
+        run.step_call(0)
+    ms = run.isolated(run.step_call, args.steps)
+    st, flags = run.device_error()
+    assert st == 0 and flags == 0, f"device error word {flags:#x}"
+    print(json.dumps({"profile_run": args.workload, "steps": args.steps, "warmup": args.warmup,
+                      "step_us_mean": statistics.mean(ms) * 1e3}), flush=True)
+    run.close()
 
 
 def _oracle_setup(wl, n_seq, n_q=1):
@@ -386,33 +572,80 @@ def _oracle_setup(wl, n_seq, n_q=1):
     return o, sub, rows
 
 
-def _oracle_step(wl, o, sub, rows, n_q=1, q_multi=None):
-    st = o.append(*sub)
+def _oracle_append(o, sub):
+    assert o.append(*sub) == 0
+
+
+def _oracle_decode(wl, o, rows, n_q=1, q_multi=None):
     if n_q == 1:
-        out, st2 = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+        out, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
     else:
-        out, st2 = o.decode_multi(q_multi, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
-    assert st == 0 and st2 == 0
+        out, st = o.decode_multi(q_multi, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    assert st == 0
     return out
 
 
-def cpu_baseline(wl, n_seq, n_q=1):
+def _sample_bytes(wl, n_seq, n_q):
+    """Algorithmic bytes of the decode restricted to the first n_seq sequences."""
+    from paged_gqa_decode_02_gb300.metrics import decode_bytes
+
+    class _Sub:
+        pass
+    s = _Sub()
+    s.batch, s.num_q_heads, s.num_kv_heads = n_seq, wl.num_q_heads, wl.num_kv_heads
+    s.head_dim, s.block_size, s.kv_dtype = wl.head_dim, wl.block_size, wl.kv_dtype
+    s.seq_lens, s.block_table = wl.seq_lens[:n_seq], wl.block_table[:n_seq]
+    return decode_bytes(s, n_q)["algorithmic"]
+
+
+def _time_oracle(wl, o, sub, rows, n_q, qm, budget_s, max_reps):
+    """Mean append and decode times of the oracle over up to max_reps steps."""
+    _oracle_append(o, sub)
+    _oracle_decode(wl, o, rows, n_q, qm)
+    t_app, t_dec, reps, t0 = 0.0, 0.0, 0, time.perf_counter()
+    while True:
+        a = time.perf_counter()
+        _oracle_append(o, sub)
+        b = time.perf_counter()
+        _oracle_decode(wl, o, rows, n_q, qm)
+        c = time.perf_counter()
+        t_app += b - a
+        t_dec += c - b
+        reps += 1
+        if c - t0 > budget_s or reps >= max_reps:
+            break
+    return t_app / reps, t_dec / reps, reps
+
+
+def cpu_baseline(name, n_seq, n_q=1):
+    """The oracle (fp64, scalar C) on this host's cores: all of them, and one."""
     from oracle import oracle
     from paged_gqa_decode_02_gb300 import workloads as W
+    wl = W.CONFIGS[name]()
     n_seq = min(n_seq, wl.batch)
     o, sub, rows = _oracle_setup(wl, n_seq, n_q)
     qm = None if n_q == 1 else W.multi_token_queries(100, wl.batch, n_q, wl.num_q_heads, wl.head_dim)
-    _oracle_step(wl, o, sub, rows, n_q, qm)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        _oracle_step(wl, o, sub, rows, n_q, qm)
-        reps += 1
-        if time.perf_counter() - t0 > 10.0 or reps >= 20:
-            break
-    t = (time.perf_counter() - t0) / reps
-    return {"value": n_seq * n_q / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    ta, td, reps = _time_oracle(wl, o, sub, rows, n_q, qm, 8.0, 20)
+    # one thread: a smaller sample (a quarter of the sequences, at least one)
+    n1 = max(1, n_seq // 4)
+    o1, sub1, rows1 = _oracle_setup(wl, n1, n_q)
+    oracle.set_num_threads(1)
+    try:
+        ta1, td1, reps1 = _time_oracle(wl, o1, sub1, rows1, n_q, qm, 8.0, 5)
+    finally:
+        oracle.set_num_threads(cores)
+    nbytes = _sample_bytes(wl, n_seq, n_q)
+    nbytes1 = _sample_bytes(wl, n1, n_q)
+    return {"value": n_seq * n_q / (ta + td), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": _cpu_model(),
+            "append_ms": ta * 1e3, "decode_ms": td * 1e3, "decode_gbs": nbytes / td / 1e9,
+            "single_thread": {"value": n1 * n_q / (ta1 + td1), "unit": "tokens/s", "cores": 1,
+                              "append_ms": ta1 * 1e3, "decode_ms": td1 * 1e3, "decode_gbs": nbytes1 / td1 / 1e9,
+                              "sample": f"{n1} of {wl.batch} sequences, mean of {reps1} steps"},
             "sample": f"{n_seq} of {wl.batch} sequences (all {wl.num_q_heads} heads and {n_q} query token(s) "
-                      f"each), append + decode step, mean of {reps} steps"}
+                      f"each), append + decode step, mean of {reps} steps; GB/s over the sample's "
+                      f"algorithmic bytes ({nbytes / 1e6:.1f} MB)"}
 
 
 def run_reference(args):
@@ -429,32 +662,49 @@ def run_reference(args):
     qm = None if n_q == 1 else W.multi_token_queries(100, wl.batch, n_q, wl.num_q_heads, wl.head_dim)
     o, sub, rows = _oracle_setup(wl, n_seq, n_q)
     for _ in range(max(3, args.warmup)):
-        _oracle_step(wl, o, sub, rows, n_q, qm)
+        _oracle_append(o, sub)
+        _oracle_decode(wl, o, rows, n_q, qm)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step(wl, o, sub, rows, n_q, qm)
+        _oracle_append(o, sub)
+        _oracle_decode(wl, o, rows, n_q, qm)
         times.append(time.perf_counter() - t0)
         if sum(times) > 120:
             break
     t = statistics.mean(times)
     v = n_seq * n_q / t
+    cfg, _ = workload_config(wl, args.workload, n_q, world)
     res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
            "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quantisation steps)",
-           "data": "synthetic (same seeded workload)",
-           "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "query_tokens": n_q},
+           "data": "synthetic (same seeded workload)", "config": cfg,
            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                            "cpu_model": _cpu_model(),
                             "sample": f"{n_seq} of {wl.batch} sequences per step (all heads, {n_q} query "
                                       f"token(s) each), append + decode"},
            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
 
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _launch_ranks(n):
+    """Start n local ranks of this script (one per GPU) and pass their output
+    through; rank 0 prints the JSON line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.run(cmd, cwd=ROOT).returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen25_7b_bf16", choices=sorted(WORKLOAD_TEXT))
@@ -469,9 +719,18 @@ def main():
     ap.add_argument("--query-tokens", type=int, default=1,
                     help="causal query tokens per sequence (chunked prefill / speculative verification)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the headline workload only")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="only W warm-up and K isolated steps of --workload (one pool, no other timings): "
+                         "the short, fixed launch sequence that profiler captures use")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(_launch_ranks(args.gpus))
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile_run:
+        profile_run(args)
     else:
         run_ours(args)
 

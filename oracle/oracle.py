@@ -86,11 +86,18 @@ def lib():
             _lib.oracle_e4m3_value.restype = ctypes.c_double
             _lib.oracle_num_threads.argtypes = []
             _lib.oracle_num_threads.restype = i32
+            _lib.oracle_set_num_threads.argtypes = [i32]
+            _lib.oracle_set_num_threads.restype = None
         return _lib
 
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (timing only)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def _p(a):

@@ -72,6 +72,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads the OpenMP loops below use from now on (n >= 1); a timing knob for
+   the benchmark's CPU baseline, with no effect on any result. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 static float bf16_to_float(uint16_t b) {
   uint32_t u = ((uint32_t)b) << 16;
   float f;

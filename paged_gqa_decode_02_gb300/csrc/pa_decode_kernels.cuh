@@ -1745,19 +1745,6 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   pdl_launch_dependents();
   // the TMA descriptor is fetched while the plan runs
   if (tid == 0 && p.maps.valid) prefetch_tensormap(&p.maps.rec);
-  // the block table -> L2, each thread block a share of it, so that the
-  // staging of its entries below (after the plan) finds them there. Whole
-  // 16-byte words inside the table only. A prefetch is a hint: it is safe
-  // before the wait on the preceding kernel whatever that kernel writes.
-  if (tid == 32 && p.batch > 0) {
-    const int rows = MQ ? p.batch / p.n_cg : p.batch;  // real sequences (table rows)
-    const unsigned long long bytes = (unsigned long long)rows * (unsigned long long)p.max_blocks * 4ull;
-    const unsigned long long base = reinterpret_cast<unsigned long long>(p.block_table);
-    unsigned long long a = (base + bytes * (unsigned long long)cta / (unsigned long long)Gc + 15ull) & ~15ull;
-    const unsigned long long e = (base + bytes * (unsigned long long)(cta + 1) / (unsigned long long)Gc) & ~15ull;
-    for (; a < e; a += 32768ull)
-      prefetch_l2_bulk(reinterpret_cast<const void*>(a), (uint32_t)min(32768ull, e - a));
-  }
   bool waited = false;
   if (!p.early_plan) {
     pdl_wait();
@@ -2379,14 +2366,14 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
 // With MQ (several query tokens per sequence) the units are those of the
 // virtual sequences (see DecodeParams): lengths come from sequence b / n_cg
 // and column c of a unit goes to its own row.
-// Four warps (one per SM sub-partition) and at most 112 registers a thread:
-// small enough to share an SM with a decode thread block, whose two warps on
-// one sub-partition take 12.8 K of its 16 K registers, so the combine of one
-// call and the decode of the next can both be resident. Launched with
-// kCombineThreads threads.
-constexpr int kCombineThreads = 128;
+// Launched with kCombineThreads threads, one four-channel quad of the unit's
+// columns each (at most 8 columns of 128 channels). (A four-warp variant at
+// 112 registers, which fits beside a decode thread block on one SM, measured
+// 0.3 us faster back to back but 0.5 us slower per isolated call, and made
+// the decode step no faster.)
+constexpr int kCombineThreads = 256;
 template <int D, bool MQ = false>
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kCombineThreads)
     splitkv_combine_kernel(const int32_t* seq_lens, const int32_t* pre_cost, const float* part_o,
                            const float* part_lse, float* out, int batch, int num_kv_heads, int group,
                            int num_q_heads, int num_ctas, int block_size, int max_blocks, int unit_cost,
@@ -2485,9 +2472,9 @@ __global__ void __maxnreg__(112)
     return;
   }
   if (usl.first == usl.last) return;
-  // this thread's quads: four channels of one column each, quads tid and
-  // tid + 128 of the unit's cols * D / 4 (at most 256: 8 columns of 128)
-  constexpr int kQ = 2;
+  // this thread's quads: four channels of one column each, quads tid,
+  // tid + kCombineThreads, ... of the unit's cols * D / 4 (at most 256)
+  constexpr int kQ = (256 + kCombineThreads - 1) / kCombineThreads;
   const int nquad = cols * D / 4;
   if (tid >= nquad) return;
   int e0[kQ], hq[kQ];

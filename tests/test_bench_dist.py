@@ -61,3 +61,33 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert res["impl"] == "reference" and res["n_gpus"] == 2 and res["steps"] == 2
     assert res["value"] > 0 and res["e2e"]["value"] == res["value"]
     assert res["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gpus_flag_starts_the_ranks_itself():
+    """--gpus 2 without a torchrun environment: the script starts two local
+    ranks (rendezvous on 127.0.0.1) and prints one line with n_gpus 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["OMP_NUM_THREADS"] = "2"
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--gpus", "2",
+           "--steps", "2", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    res = json.loads(lines[0])
+    assert res["impl"] == "reference" and res["n_gpus"] == 2
+    assert res["config"]["parallelism"] == "replicas x2 (no exchange)"
+
+
+def test_reference_arm_prints_the_workload_config_of_the_gpu_arm():
+    """Both arms describe the workload with the same config dict."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_gqa_decode_02_gb300 import workloads as W
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, OMP_NUM_THREADS="2"))
+    assert r.returncode == 0, r.stderr[-3000:]
+    res = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    cfg, _ = bench.workload_config(W.CONFIGS["tiny"](), "tiny", 1, 1)
+    assert res["config"] == cfg
