@@ -225,7 +225,10 @@ PA_API int32_t pa_decode_num_splits(const pa_pool* pool, int32_t num_splits);
  * the same operation. Sequences cut by slice boundaries are merged by a
  * separate log-sum-exp combine kernel; OR-ing PA_DECODE_FUSED_COMBINE merges
  * them inside the decode kernel instead (the last slice to finish a sequence
- * merges its partials, found through call-tagged tickets). OR-ing
+ * merges its partials, found through call-tagged tickets that it clears once
+ * it has merged, so a CUDA graph that replays the call finds them zero again;
+ * after a call that reported PA_DEVERR_TIMEOUT, zero the workspace again
+ * before the next call with this option). OR-ing
  * PA_DECODE_EARLY_PLAN lets the decode kernel read seq_lens and block_table
  * (and plan its work) while the kernel launched just before it on the stream
  * is still running; it still waits for that kernel before reading any page or

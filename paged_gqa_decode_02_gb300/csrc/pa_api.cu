@@ -534,6 +534,13 @@ extern "C" pa_status pa_decode_noalloc(pa_pool* p, const void* q, const int32_t*
                                        int32_t num_splits, void* stream) {
   g_last_error[0] = 0;
   if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
+  // Argument errors and the empty batch get pa_decode's own answer, before the
+  // scratch's address is looked up (which selects the device and loads the
+  // module): such a call has no side effect.
+  if (batch <= 0 || num_q_heads < 1 || num_splits < 0 || max_blocks <= 0 || !isfinite(softmax_scale) || !q ||
+      !block_table || !seq_lens || !out)
+    return pa_decode(p, q, block_table, seq_lens, batch, num_q_heads, max_blocks, softmax_scale, out, nullptr, 0,
+                     num_splits, stream);
   const int dev = p->desc.device;
   if (dev >= kNoAllocMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device ordinal above 63%s");
   const size_t need = pa_decode_workspace_bytes(p, batch, num_q_heads, num_splits);

@@ -94,9 +94,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, giving up after
-// roughly `limit_cycles` SM clocks. Returns false on timeout.
+// roughly `limit_cycles` SM clocks. Returns false on timeout. The default,
+// 2e8 clocks (about 0.1 s at 2 GHz), is far above the longest wait of a
+// healthy launch: every wait starts after the wait on the preceding kernel,
+// and the longest, the merger's wait for a slice's first unit, covers at most
+// one slice's pages (a slice of 100 k pages streams in about 20 ms).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  long long limit_cycles = 4000000000LL) {
+                                                  long long limit_cycles = 200000000LL) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {

@@ -129,7 +129,7 @@ struct DecodeParams {
   int32_t* pre_cost;             // [batch + 1] per-head cost-line prefix of the sequences
   float* part_o;
   float* part_lse;
-  unsigned long long* tickets;  // per unit: (epoch << 24) | slices finished
+  unsigned long long* tickets;  // per unit: (epoch << 24) | slices finished; 0 once merged
   unsigned long long epoch;     // 40-bit call tag, never 0
   int fused;                    // merge split units in this kernel (else: combine kernel)
   int early_plan;               // plan (reads of lengths / tables only) before waiting
@@ -2330,6 +2330,10 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           if (last_slice) {
             __threadfence();
             merge_unit_partials<D>(usl, u, row0, g, p.part_o, p.part_lse, p.out, lane, 32);
+            // every slice of the unit has taken its ticket: clear it, so that a
+            // replay of this very launch (a CUDA graph keeps its epoch) starts
+            // from zero again
+            if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(p.tickets + u) = 0ull;
           }
         }
       }

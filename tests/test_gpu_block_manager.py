@@ -128,3 +128,47 @@ def test_decode_step_replays_from_a_cuda_graph():
         assert torch.equal(out, ref)
     assert g.device_error() == (0, 0)
     g.close()
+
+
+def test_fused_combine_replays_from_a_cuda_graph_with_new_queries():
+    """The in-kernel merge (PA_DECODE_FUSED_COMBINE) captured in a CUDA graph:
+    every replay keeps the captured call's ticket tag, so the merging slice
+    must leave its tickets cleared. New queries are copied into the captured
+    buffer before each replay and every replay must match the oracle for them
+    (a stale ticket would leave split rows unmerged, holding the last replay's
+    values)."""
+    torch = H.torch_mod()
+    wl = W.make_case("graph_fused", 13, 6, 28, 4, 128, 16, "bf16", [700, 33, 1500, 1, 257, 4096], extra_blocks=2)
+    g, o = H.load_both(wl, leave_last=False)
+    g.set_decode_path("auto", fused_combine=True, early_plan=False)
+    table, lens = H.dev(wl.block_table), H.dev(wl.seq_lens)
+    q = H.dev(wl.q_bits)
+    out = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
+    ws = g.workspace(wl.batch, wl.num_q_heads)
+
+    def call():
+        g.decode(q, table, lens, wl.softmax_scale, out=out, workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    rng = np.random.default_rng(77)
+    for r in range(3):
+        qb = W.f32_to_bf16_bits(rng.standard_normal(wl.q_bits.shape, dtype=np.float32))
+        q.copy_(H.dev(qb))
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref, st = o.decode(qb, wl.block_table, wl.seq_lens, wl.softmax_scale)
+        assert st == 0
+        H.check_attention(out.cpu().numpy().reshape(-1, wl.head_dim), ref, f"fused graph replay {r}")
+    assert g.device_error() == (0, 0)
+    g.close()

@@ -161,20 +161,19 @@ FULL = ["qwen25_7b_bf16", "qwen3_8b_int8", "long_uint4", "prefix_mix", "qwen3_8b
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_config(name):
     """Full-size workloads: the whole pool bit-exact after the bulk append and
-    the decode step's append; attention on sampled rows, in the automatic
+    the decode step's append; attention on every output row (the oracle,
+    OpenMP over the host's cores, computes them all), in the automatic
     launch configuration the benchmark times and with one forced split count."""
     wl = W.CONFIGS[name]()
     g, o = H.load_both(wl)
     H.assert_pools_equal(g, o)
-    rows = H.sample_rows(wl)
-    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale, rows=rows)
+    ref, st = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)
     assert st == 0
     for path in _paths(wl.kv_dtype, wl.head_dim):
         for splits, combine, early in ((0, "fused", False), (97, "fused", True), (0, "separate", True),
                                        (0, "separate", False)):
             got = H.gpu_decode(g, wl, num_splits=splits, path=path, combine=combine, early_plan=early)
-            H.check_attention(got[rows], ref, f"{name} splits={splits} {path} {combine} early={early}")
-            assert np.isfinite(got).all()
+            H.check_attention(got, ref, f"{name} splits={splits} {path} {combine} early={early}")
     assert g.device_error() == (0, 0)
 
 

@@ -47,8 +47,10 @@ def test_noalloc_matches_decode_twice(lib, dt, splits):
     torch = H.torch_mod()
     wl = W.make_case("noalloc", 90, 3, 28, 4, 128, 16, dt, [700, 33, 1500], extra_blocks=2,
                      channel_offset_sigma=0.5 if dt != "bf16" else None)
-    g, _ = H.load_both(wl)
+    g, o = H.load_both(wl)
     ref = H.gpu_decode(g, wl, num_splits=splits)  # pa_decode with a caller workspace
+    oref, ost = o.decode(wl.q_bits, wl.block_table, wl.seq_lens, wl.softmax_scale)  # the CPU oracle
+    assert ost == 0
     q, table, lens = H.dev(wl.q_bits), H.dev(wl.block_table), H.dev(wl.seq_lens)
     for call in range(2):
         out = torch.full((wl.batch, wl.num_q_heads, wl.head_dim), float("nan"), dtype=torch.float32,
@@ -58,7 +60,19 @@ def test_noalloc_matches_decode_twice(lib, dt, splits):
         torch.cuda.synchronize()
         got = out.cpu().numpy().reshape(ref.shape)
         H.check_attention(got, ref.astype(np.float64), f"noalloc call {call} {dt} splits={splits}")
+        H.check_attention(got, oref, f"noalloc call {call} {dt} splits={splits} against the oracle")
     assert g.device_error() == (0, 0)
+    g.close()
+
+
+def test_noalloc_empty_and_invalid_calls_answer_like_decode(lib):
+    """An empty batch returns PA_OK and invalid arguments get pa_decode's
+    error, both before the scratch is looked up (nothing launched)."""
+    wl = W.make_case("noalloc_args", 92, 2, 8, 8, 128, 16, "bf16", [16, 16])
+    g, _ = H.make_pools(wl)
+    assert lib.pa_decode_noalloc(g.handle, None, None, None, 0, 8, 1, 0.125, None, 0, None) == 0
+    assert lib.pa_decode_noalloc(g.handle, None, None, None, -1, 8, 1, 0.125, None, 0, None) == 1
+    assert lib.pa_decode_noalloc(g.handle, None, None, None, 2, 7, 1, 0.125, None, 0, None) == 1
     g.close()
 
 
@@ -66,7 +80,10 @@ def test_noalloc_rejects_batches_beyond_its_scratch(lib):
     wl = W.make_case("noalloc_big", 91, 2, 8, 8, 128, 16, "bf16", [16, 16])
     g, _ = H.make_pools(wl)
     big_batch = 1 << 16  # scratch need far above 8 MiB; refused before any launch
-    st = lib.pa_decode_noalloc(g.handle, None, None, None, big_batch, 8, 1, 0.125, None, 0, None)
+    torch = H.torch_mod()
+    buf = torch.zeros(64, dtype=torch.float32, device="cuda")  # never read: the call is refused first
+    ptr = ctypes.c_void_p(buf.data_ptr())
+    st = lib.pa_decode_noalloc(g.handle, ptr, ptr, ptr, big_batch, 8, 1, 0.125, ptr, 0, None)
     assert st == 3
     msg = lib.pa_last_error().decode()
     assert "static scratch holds" in msg and "8388608" in msg
