@@ -207,7 +207,9 @@ __device__ __noinline__ void merge_unit_partials(const UnitSlices& us, long long
                                                  int group, const float* __restrict__ part_o,
                                                  const float* __restrict__ part_lse,
                                                  float* __restrict__ out, int tid, int nthr) {
-  constexpr int kBatch = 4, kCols = 1;
+  // four columns x two slices per round: a unit of 8 heads x 128 channels
+  // (256 float4 columns) takes two rounds of loads on one warp
+  constexpr int kBatch = 2, kCols = 4;
   const int ncol = group * D / 4;
   for (int c0 = tid; c0 < ncol; c0 += nthr * kCols) {
     float M[kCols], W[kCols], A[kCols][4];
@@ -2315,8 +2317,12 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
           int last_slice = 0;
           if (lane == 0) {
             const unsigned long long tag = p.epoch << 24;
+            const unsigned long long cnt = (unsigned long long)usl.count();  // >= 2: the unit is split
             unsigned long long* t = p.tickets + u;
-            unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(t), assumed;
+            // first guess: every other slice is done (this call's tag, cnt - 1),
+            // so the last slice, the one on the critical path, takes its ticket
+            // in one round trip; a wrong guess returns the value to retry with
+            unsigned long long old = tag | (cnt - 1), assumed;
             unsigned long long mine;
             do {
               assumed = old;
@@ -2324,7 +2330,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
               mine = done + 1;
               old = atomicCAS(t, assumed, tag | mine);
             } while (old != assumed);
-            last_slice = mine == (unsigned long long)usl.count() ? 1 : 0;
+            last_slice = mine == cnt ? 1 : 0;
           }
           last_slice = __shfl_sync(0xffffffffu, last_slice, 0);
           if (last_slice) {
