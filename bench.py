@@ -18,8 +18,9 @@ whole job over all ranks. Two timings of each workload:
   back_to_back  K steps (calls) in one pair of events, each reading another
                 of several copies of the pool (every copy larger than L2), as
                 a decoding loop issues them.
-`stream_ceiling` times a plain read of the same number of bytes both ways: it
-is what the launch, ramp-up and drain of one kernel cost at this size.
+`stream_ceiling` times the simplest read of the same number of bytes both ways
+(pa_stream_read): what the launch, ramp-up and drain of one kernel cost at
+this size.
 
 With --gpus N > 1 and no torchrun environment the script starts N local
 ranks itself (torch.distributed.run, 127.0.0.1). Every rank runs its own
@@ -421,37 +422,40 @@ def measure(run, dist, world, K, warmup, peak, peak_kind, K_e2e):
 
 
 def stream_ceiling(dev, nbytes, K):
-    """A plain read of `nbytes` (torch's sum over a float32 buffer), timed like
-    the decode call: isolated with the L2 flushed, and back to back over three
+    """The simplest kernel that reads `nbytes` (the library's calibration read,
+    pa_stream_read: 16-byte streaming loads over every SM), timed like the
+    decode call: isolated with the L2 flushed, and back to back over three
     copies. What one kernel's launch, ramp-up and drain cost at this size."""
     import torch
-    n = max(1, nbytes // 4)
-    bufs = [torch.ones(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    from paged_gqa_decode_02_gb300 import binding
+    n = max(16, (nbytes + 15) // 16 * 16)
+    bufs = [torch.ones(n // 4, dtype=torch.float32, device=dev) for _ in range(3)]
+    sink = torch.zeros(4, dtype=torch.int32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for b in bufs:
-        b.sum()
-    ms = []
+        binding.pa_stream_read(b, sink)
+    ev = []
     for i in range(K):
         flush.fill_(1)
         a = torch.cuda.Event(enable_timing=True)
         z = torch.cuda.Event(enable_timing=True)
         a.record()
-        bufs[0].sum()
+        binding.pa_stream_read(bufs[0], sink)
         z.record()
-        ms.append((a, z))
+        ev.append((a, z))
     torch.cuda.synchronize()
-    iso = statistics.mean(a.elapsed_time(z) for a, z in ms) / 1e3
+    iso = statistics.mean(a.elapsed_time(z) for a, z in ev) / 1e3
     a = torch.cuda.Event(enable_timing=True)
     z = torch.cuda.Event(enable_timing=True)
     a.record()
     for i in range(K):
-        bufs[i % 3].sum()
+        binding.pa_stream_read(bufs[i % 3], sink)
     z.record()
     torch.cuda.synchronize()
     b2b = a.elapsed_time(z) / K / 1e3
-    return {"bytes": n * 4, "isolated_us": iso * 1e6, "isolated_gbs": n * 4 / iso / 1e9,
-            "back_to_back_us": b2b * 1e6, "back_to_back_gbs": n * 4 / b2b / 1e9,
-            "kernel": "torch.sum over a float32 buffer (a read of the same bytes)"}
+    return {"bytes": n, "isolated_us": iso * 1e6, "isolated_gbs": n / iso / 1e9,
+            "back_to_back_us": b2b * 1e6, "back_to_back_gbs": n / b2b / 1e9,
+            "kernel": "pa_stream_read: 16-byte streaming loads over every SM, nothing else (a read of the same bytes)"}
 
 
 def run_ours(args):

@@ -275,6 +275,20 @@ PA_API pa_status pa_get_device_error(pa_pool* pool, void* stream, uint32_t* flag
  * [1, 4e9]; nothing launched), PA_ERR_CUDA. */
 PA_API pa_status pa_selftest_wait_timeout(int32_t device, int64_t limit_cycles, uint32_t* flags);
 
+/* Bandwidth calibration, not part of the decode path: read `bytes` bytes at
+ * `src` with 16-byte streaming loads spread over every SM of the current
+ * device, folding them into one 32-bit word that is OR-ed into *sink only in
+ * the (practically never taken) case that it equals a fixed constant, so that
+ * no load can be dropped and nothing is written otherwise. Timed beside the
+ * decode call, it gives the time of the simplest kernel that reads the same
+ * number of bytes: the ceiling that one launch of that size can reach.
+ *   src    device, 16-byte aligned; bytes a multiple of 16
+ *   sink   device uint32_t
+ * Asynchronous on `stream` (a cudaStream_t; NULL = the default stream).
+ * Errors: PA_ERR_INVALID_ARG (null pointer, misaligned src, bytes not a
+ * multiple of 16; nothing launched), PA_ERR_CUDA. */
+PA_API pa_status pa_stream_read(const void* src, size_t bytes, uint32_t* sink, void* stream);
+
 /* Static description of a status code. */
 PA_API const char* pa_status_string(pa_status s);
 

@@ -106,6 +106,8 @@ def lib():
         L.pa_copy_blocks.restype = I32
         L.pa_selftest_wait_timeout.argtypes = [I32, I64, ctypes.POINTER(ctypes.c_uint32)]
         L.pa_selftest_wait_timeout.restype = I32
+        L.pa_stream_read.argtypes = [P, SZ, P, P]
+        L.pa_stream_read.restype = I32
         L.pa_pool_block_bytes.argtypes = [P]
         L.pa_pool_block_bytes.restype = ctypes.c_size_t
         L.pa_swap_blocks.argtypes = [P, P, I32, P, P, I32, I32, P]
@@ -197,6 +199,13 @@ def pa_pool_set_unit_cost(handle, unit_cost_pages):
 
 def pa_decode_num_splits(handle, num_splits=0):
     return int(lib().pa_decode_num_splits(handle, int(num_splits)))
+
+
+def pa_stream_read(src, sink, stream=None):
+    """Bandwidth calibration: read the whole of tensor `src` (16-byte aligned,
+    its size a multiple of 16 bytes) with the simplest streaming kernel; `sink`
+    is a device int32 tensor. Asynchronous."""
+    _check(lib().pa_stream_read(_ptr(src), src.numel() * src.element_size(), _ptr(sink), _stream(stream)))
 
 
 def pa_get_device_error(handle, stream=None):

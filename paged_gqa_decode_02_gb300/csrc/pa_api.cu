@@ -307,6 +307,34 @@ pa_status pa_selftest_wait_timeout(int32_t device, int64_t limit_cycles, uint32_
   return PA_OK;
 }
 
+// The bandwidth calibration read: grid-stride 16-byte streaming loads, XOR
+// folded per thread; the fold is stored only if it equals a constant.
+__global__ void __launch_bounds__(512) stream_read_kernel(const int4* __restrict__ src, size_t n16,
+                                                          uint32_t* sink) {
+  uint32_t acc = 0;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+    const int4 v = __ldcs(src + i);
+    acc ^= (uint32_t)(v.x ^ v.y ^ v.z ^ v.w);
+  }
+  if (acc == 0x9E3779B9u) atomicOr(sink, acc);
+}
+
+pa_status pa_stream_read(const void* src, size_t bytes, uint32_t* sink, void* stream) {
+  g_last_error[0] = 0;
+  if (!src || !sink || !aligned16(src) || (bytes & 15u))
+    return fail(PA_ERR_INVALID_ARG, "null pointer, src not 16-byte aligned or bytes not a multiple of 16%s");
+  if (bytes == 0) return PA_OK;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  stream_read_kernel<<<4 * sms, 512, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const int4*>(src),
+                                                                              bytes / 16, sink);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "stream_read launch");
+  return PA_OK;
+}
+
 pa_status pa_get_device_error(pa_pool* p, void* stream, uint32_t* flags) {
   g_last_error[0] = 0;
   if (!p || !flags) return fail(PA_ERR_INVALID_ARG, "null pool or flags%s");

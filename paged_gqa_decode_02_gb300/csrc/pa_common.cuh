@@ -250,8 +250,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Two bytes of w (chosen by sel, see prmt) as two exact f16 integers 0..255:
-// 0x64XX is the f16 value 1024 + XX, minus 1024.
+// Two bytes of w (chosen by sel, see prmt) as two exact f16 integers 0..255.
+// The IEEE-754 binary16 identity behind it: exponent field 25 (bias 15, so a
+// scale of 2^10) with ten mantissa bits m is the value 1024 + m, so the bit
+// pattern 0x6400 | XX is exactly 1024 + XX, and one f16 subtraction of 1024
+// (exact: both operands are integers below 2048) leaves XX. This is the
+// usual bit-level integer-to-half conversion of low-precision dequantisation
+// kernels, here written from the format's definition.
 __device__ __forceinline__ uint32_t bytes_to_f16x2(uint32_t w, uint32_t sel) {
   const uint32_t x = prmt(w, 0x64646464u, sel);
   __half2 h = *reinterpret_cast<const __half2*>(&x);

@@ -64,6 +64,11 @@ def test_null_pool_arguments(lib):
     assert lib.pa_pool_block_bytes(None) == 0
     assert lib.pa_selftest_wait_timeout(0, 0, ctypes.byref(f)) == 1  # refused before any launch
     assert lib.pa_selftest_wait_timeout(0, 1000, None) == 1
+    # the calibration read refuses null, misaligned or ragged arguments before any launch
+    assert lib.pa_stream_read(None, 16, ctypes.byref(f), None) == 1
+    assert lib.pa_stream_read(ctypes.c_void_p(16), 16, None, None) == 1
+    assert lib.pa_stream_read(ctypes.c_void_p(8), 16, ctypes.byref(f), None) == 1
+    assert lib.pa_stream_read(ctypes.c_void_p(16), 24, ctypes.byref(f), None) == 1
 
 
 def test_null_block_manager_arguments(lib):

@@ -27,3 +27,14 @@ def test_a_wait_that_cannot_complete_reports_and_the_gpu_stays_usable():
     H.check_attention(H.gpu_decode(g, wl), ref, "decode after an expired wait")
     assert g.device_error() == (0, 0)
     g.close()
+
+
+def test_stream_read_calibration_runs_and_writes_nothing():
+    """pa_stream_read (the benchmark's bandwidth calibration) reads a buffer
+    and leaves the sink alone unless the fold hits its constant."""
+    torch = H.torch_mod()
+    buf = torch.ones(1 << 20, dtype=torch.float32, device="cuda")
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    B.pa_stream_read(buf, sink)
+    torch.cuda.synchronize()
+    assert int(sink[0].item()) == 0
