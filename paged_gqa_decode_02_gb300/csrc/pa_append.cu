@@ -32,15 +32,46 @@ __device__ __forceinline__ int read_code(const uint8_t* page_codes, int D, int s
   return (c & 1) ? (byte >> 4) : (byte & 15);
 }
 
-// One thread block per (sequence, touched-block slot x, tensor/head z); one
-// thread per channel. grid = (X, batch, 2 * Hkv), block = head_dim threads.
+// Lanes per channel: the tokens of a block are spread over tok_lanes<BS>()
+// lanes (token s goes to lane s % lanes), 8 tokens a thread, so a thread
+// quantises 8 tokens instead of all BS and the per-channel min / max is a
+// shuffle reduction over the lanes. Eight keeps a decode step's append (one
+// block per sequence, K and V of every kv head) within one wave of threads:
+// batch 64 x 8 kv heads x 2 x 256 threads for 16-token blocks.
+template <int BS>
+constexpr int tok_lanes() {
+  return BS / 8;
+}
+
+// min / max over the lanes of one channel, with the sequential rule of the
+// quantiser: the running value starts at token 0 and a token replaces it only
+// when it compares below (above); so a NaN counts only as token 0, and the
+// other values give the same result in any order (+-0 ties change neither
+// the scale nor the zero point).
+template <int TL>
+__device__ __forceinline__ void channel_min_max(float& mn, float& mx, float v0) {
+#pragma unroll
+  for (int o = 1; o < TL; o <<= 1) {
+    const float a = __shfl_xor_sync(0xffffffffu, mn, o), b = __shfl_xor_sync(0xffffffffu, mx, o);
+    if (a < mn) mn = a;
+    if (b > mx) mx = b;
+  }
+  if (v0 != v0) mn = mx = v0;  // token 0 is NaN
+}
+
+// One thread block per (sequence, touched-block slot x, tensor/head z); a
+// warp holds 32 / kTokLanes channels x kTokLanes token lanes.
+// grid = (X, batch, 2 * Hkv), block = head_dim * kTokLanes threads.
 template <int KV, int BS>
-__global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv_bfloat16* k_new,
-                                                        const __nv_bfloat16* v_new,
-                                                        const int32_t* cu_new,
-                                                        const int32_t* ctx_lens,
-                                                        const int32_t* block_table,
-                                                        int32_t max_blocks) {
+__global__ void __launch_bounds__(128 * tok_lanes<BS>()) kv_append_kernel(PoolDev pool, const __nv_bfloat16* k_new,
+                                                                    const __nv_bfloat16* v_new,
+                                                                    const int32_t* cu_new,
+                                                                    const int32_t* ctx_lens,
+                                                                    const int32_t* block_table,
+                                                                    int32_t max_blocks) {
+  constexpr int kTokLanes = tok_lanes<BS>();
+  constexpr int NJ = BS / kTokLanes;  // tokens per thread: s = ts + kTokLanes * j
+  static_assert(BS % kTokLanes == 0 && kTokLanes >= 1 && kTokLanes <= 32, "token lanes");
   // programmatic stream serialization: start early, touch memory only after
   // the preceding kernel has completed
   pdl_launch_dependents();
@@ -48,21 +79,24 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
   const int b = blockIdx.y;
   const int is_v = blockIdx.z & 1;
   const int h = blockIdx.z >> 1;
-  const int c = threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int ts = lane & (kTokLanes - 1);
+  const int c = (threadIdx.x >> 5) * (32 / kTokLanes) + (lane / kTokLanes);  // channel
   const int D = pool.head_dim;
   const int Hkv = pool.num_kv_heads;
+  const bool lead = threadIdx.x == 0;
 
   const int32_t c0 = cu_new[b], c1 = cu_new[b + 1];
   const int n_new = c1 - c0;
   if (n_new < 0) {
-    if (blockIdx.x == 0 && c == 0 && blockIdx.z == 0) set_error(pool.err, PA_DEVERR_APPEND);
+    if (blockIdx.x == 0 && lead && blockIdx.z == 0) set_error(pool.err, PA_DEVERR_APPEND);
     return;
   }
   if (n_new == 0) return;
   const int ctx = ctx_lens[b];
   const long long total = (long long)ctx + n_new;
   if (ctx < 0 || total > (long long)max_blocks * BS) {
-    if (blockIdx.x == 0 && c == 0 && blockIdx.z == 0) set_error(pool.err, PA_DEVERR_SEQ_LEN);
+    if (blockIdx.x == 0 && lead && blockIdx.z == 0) set_error(pool.err, PA_DEVERR_SEQ_LEN);
     return;
   }
   const int first_blk = ctx / BS;
@@ -75,7 +109,7 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
   for (int blk = first_blk + blockIdx.x; blk <= last_blk; blk += gridDim.x) {
     const int phys = block_table[(long long)b * max_blocks + blk];
     if (phys < 0 || phys >= pool.num_blocks) {
-      if (c == 0 && !is_v && h == 0) set_error(pool.err, PA_DEVERR_BLOCK_TABLE);
+      if (lead && !is_v && h == 0) set_error(pool.err, PA_DEVERR_BLOCK_TABLE);
       continue;
     }
     const int first = blk * BS;
@@ -88,8 +122,11 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
     if (KV == PA_KV_BF16) {
       uint16_t* dst = reinterpret_cast<uint16_t*>(page_of(codes, page, pool.stride));
       const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
-      for (int s = old_cnt; s < valid; ++s)
-        dst[s * D + c] = s16[((row0 + s) * Hkv + h) * D + c];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int s = ts + kTokLanes * j;
+        if (s >= old_cnt && s < valid) dst[s * D + c] = s16[((row0 + s) * Hkv + h) * D + c];
+      }
       continue;
     }
 
@@ -98,25 +135,36 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
       uint8_t* pc = page_of(codes, page, pool.stride);
       float* psc = page_of(scales, page, pool.stride);
       const float old_scale = psc[c];
-      float vals[BS];
+      float vals[NJ];
       float amax = 0.0f;
 #pragma unroll
-      for (int s = 0; s < BS; ++s) {
+      for (int j = 0; j < NJ; ++j) {
+        const int s = ts + kTokLanes * j;
         float x = 0.0f;
         if (s < old_cnt) {
           x = __fmul_rn(e4m3_to_float(pc[s * D + c]), old_scale);
         } else if (s < valid) {
           x = __bfloat162float(src[((row0 + s) * Hkv + h) * D + c]);
         }
-        vals[s] = x;
+        vals[j] = x;
         if (s < valid && fabsf(x) > amax) amax = fabsf(x);
+      }
+#pragma unroll
+      for (int o = 1; o < kTokLanes; o <<= 1) {
+        const float a = __shfl_xor_sync(0xffffffffu, amax, o);
+        if (a > amax) amax = a;
       }
       float scale = __fdiv_rn(amax, 448.0f);
       if (!(scale > 0.0f)) scale = 1.0f;
+      // (a channel's lanes, and so every reader of its old codes and scale,
+      // are in one warp: the shuffles above ordered those reads first)
+      __syncwarp();
 #pragma unroll
-      for (int s = 0; s < BS; ++s)
-        if (s < valid) pc[s * D + c] = float_to_e4m3(__fdiv_rn(vals[s], scale));
-      psc[c] = scale;
+      for (int j = 0; j < NJ; ++j) {
+        const int s = ts + kTokLanes * j;
+        if (s < valid) pc[s * D + c] = float_to_e4m3(__fdiv_rn(vals[j], scale));
+      }
+      if (ts == 0) psc[c] = scale;
       continue;
     }
 
@@ -124,11 +172,13 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
     uint8_t* pc = page_of(codes, page, pool.stride);
     float* psc = page_of(scales, page, pool.stride);
     int32_t* pzp = page_of(zps, page, pool.stride);
-    float vals[BS];
+    float vals[NJ];
     const float old_scale = psc[c];
     const int32_t old_zp = pzp[c];
+    float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < BS; ++s) {
+    for (int j = 0; j < NJ; ++j) {
+      const int s = ts + kTokLanes * j;
       float x = 0.0f;
       if (s < old_cnt) {
         const int32_t diff = read_code<KV>(pc, D, s, c) - old_zp;
@@ -136,16 +186,14 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
       } else if (s < valid) {
         x = __bfloat162float(src[((row0 + s) * Hkv + h) * D + c]);
       }
-      vals[s] = x;
-    }
-    float mn = vals[0], mx = vals[0];
-#pragma unroll
-    for (int s = 1; s < BS; ++s) {
+      vals[j] = x;
       if (s < valid) {
-        if (vals[s] < mn) mn = vals[s];
-        if (vals[s] > mx) mx = vals[s];
+        if (x < mn) mn = x;
+        if (x > mx) mx = x;
       }
     }
+    // token 0 (always valid) is j = 0 of the channel's lane ts = 0
+    channel_min_max<kTokLanes>(mn, mx, __shfl_sync(0xffffffffu, vals[0], lane & ~(kTokLanes - 1)));
     const float r = __fsub_rn(mx, mn);
     float scale = __fdiv_rn(r, (float)L);
     if (!(scale > 0.0f)) {
@@ -153,27 +201,37 @@ __global__ void __launch_bounds__(128) kv_append_kernel(PoolDev pool, const __nv
       if (!(scale > 0.0f)) scale = 1.0f;
     }
     const int32_t zp = sat_rint_i32(rintf(__fdiv_rn(-mn, scale)));
-    int code[BS];
+    int code[NJ];
 #pragma unroll
-    for (int s = 0; s < BS; ++s) {
-      long long t = (long long)sat_rint_i32(rintf(__fdiv_rn(vals[s], scale))) + (long long)zp;
+    for (int j = 0; j < NJ; ++j) {
+      long long t = (long long)sat_rint_i32(rintf(__fdiv_rn(vals[j], scale))) + (long long)zp;
       t = t < 0 ? 0 : (t > L ? L : t);
-      code[s] = (int)t;
+      code[j] = (int)t;
     }
+    // the lanes of a channel, and of the channel sharing its uint4 bytes, are
+    // in one warp and have read their old codes, scale and zero point (the
+    // shuffles above ordered those reads before these stores)
+    __syncwarp();
     if (KV == PA_KV_UINT8) {
 #pragma unroll
-      for (int s = 0; s < BS; ++s)
-        if (s < valid) pc[s * D + c] = (uint8_t)code[s];
+      for (int j = 0; j < NJ; ++j) {
+        const int s = ts + kTokLanes * j;
+        if (s < valid) pc[s * D + c] = (uint8_t)code[j];
+      }
     } else {
-      // pair channels 2i (low nibble) and 2i+1 (high nibble) of one byte
+      // channels 2i (low nibble) and 2i+1 (high nibble) of one byte: the odd
+      // channel's lane is kTokLanes lanes up
 #pragma unroll
-      for (int s = 0; s < BS; ++s) {
-        const int other = __shfl_xor_sync(0xffffffffu, code[s], 1);
-        if (s < valid && (c & 1) == 0) pc[s * (D / 2) + c / 2] = (uint8_t)(code[s] | (other << 4));
+      for (int j = 0; j < NJ; ++j) {
+        const int s = ts + kTokLanes * j;
+        const int other = __shfl_xor_sync(0xffffffffu, code[j], kTokLanes);
+        if (s < valid && (c & 1) == 0) pc[s * (D / 2) + c / 2] = (uint8_t)(code[j] | (other << 4));
       }
     }
-    psc[c] = scale;
-    pzp[c] = zp;
+    if (ts == 0) {
+      psc[c] = scale;
+      pzp[c] = zp;
+    }
   }
 }
 
@@ -190,7 +248,7 @@ cudaError_t launch_append_t(const PoolDev& pool, const void* k_new, const void* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks_per_seq, batch, 2 * pool.num_kv_heads);
-  cfg.blockDim = dim3(pool.head_dim);
+  cfg.blockDim = dim3(pool.head_dim * tok_lanes<BS>());
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
