@@ -772,18 +772,25 @@ struct MmaConsumerU8 {
   static_assert(G <= 8, "head group");
   using PG = PageGeom<PA_KV_UINT8, 128, BS>;
 
-  uint32_t qp[16];  // q[head g] as bf16 pairs: channels 16k + 4q + {0,1} at 2k, {2,3} at 2k+1
+  // Groups of up to 4 heads (one query token) split the per-page q*scale work:
+  // lanes 16-31 prepare k-steps 4-7 of heads 0-3 and hand them to lanes 0-15
+  // by shuffle; the mma's columns 4-7 then hold values no one stores.
+  static constexpr bool kSplit = G <= 4;
+  static constexpr int KH = kSplit ? KS / 2 : KS;  // k-steps of q*scale a lane prepares
+  uint32_t qp[2 * KH];  // q[head] as bf16 pairs: channels 16k + 4q + {0,1} at 2k, {2,3} at 2k+1
   float o[8][4];    // O^T tile mt = 2p + s: rows -> channels 32p + 4g + 2s + {0, 1}
   float m0, m1, l0, l1;
   float scale_log2;
 
   __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
     const int lane = threadIdx.x & 31;
-    const int hg = lane >> 2, q4 = (lane & 3) * 4;
+    const int q4 = (lane & 3) * 4;
+    const int hg = kSplit ? (lane >> 2) & 3 : lane >> 2;
+    const int k0 = kSplit ? KH * (lane >> 4) : 0;
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
+    for (int k = 0; k < KH; ++k) {
       uint2 w = make_uint2(0, 0);
-      if (hg < g) w = *reinterpret_cast<const uint2*>(q_smem + hg * D + 16 * k + q4);
+      if (hg < g) w = *reinterpret_cast<const uint2*>(q_smem + hg * D + 16 * (k0 + k) + q4);
       qp[2 * k] = w.x;
       qp[2 * k + 1] = w.y;
     }
@@ -830,12 +837,15 @@ struct MmaConsumerU8 {
     const uint32_t bk = sb + 144 * gq + 4 * q;       // K codes, row gq
     const uint32_t bv = sb + PG::kOffV + 288 * q + 16 * (gq >> 2) + 4 * (gq & 3);  // V codes, row 2q
 
-    // ---- w = q * scale of head gq and its largest magnitude
-    float w[32];
+    // ---- w = q * scale of this lane's head (its KH k-steps) and the head's
+    // largest magnitude
+    static_assert(!(kSplit && MQ), "several query tokens use groups of 8 columns");
+    const uint32_t hx = kSplit ? 32u * (lane >> 4) : 0u, hoff = 8u * hx;  // k-steps 4-7: row phase + 2 rows
+    float w[4 * KH];
     float amax = 0.0f;
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const float4 sc = lds_f4((bq ^ (16 * (k >> 1))) + PG::kOffKs + 128 * (k >> 1) + 64 * (k & 1));
+    for (int k = 0; k < KH; ++k) {
+      const float4 sc = lds_f4(((bq ^ (16 * (k >> 1))) ^ hx) + hoff + PG::kOffKs + 128 * (k >> 1) + 64 * (k & 1));
       w[4 * k + 0] = bf16_lo(qp[2 * k]) * sc.x;
       w[4 * k + 1] = bf16_hi(qp[2 * k]) * sc.y;
       w[4 * k + 2] = bf16_lo(qp[2 * k + 1]) * sc.z;
@@ -845,6 +855,7 @@ struct MmaConsumerU8 {
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if constexpr (kSplit) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
     int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
     ex = ex < 1 ? 1 : ex;
     int sh = 140 - ex;  // 2^sh * amax lands in [2^13, 2^14)
@@ -854,16 +865,34 @@ struct MmaConsumerU8 {
 
     // ---- k-steps outermost: B = w * 2^sh split high + remainder (separate
     // accumulators keep the mma chains short), the zero-point bias, and the
-    // score mma of every 16-token tile
+    // score mma of every 16-token tile. Codes enter the mma as f16 subnormals
+    // (a byte permuted against zero into a half's mantissa is code * 2^-24,
+    // exactly), so the scores come out scaled by 2^-24.
     float sh_[TT][4], sl_[TT][4];
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) sh_[tt][i] = sl_[tt][i] = 0.0f;
+    auto qk = [&](int k, uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+#pragma unroll
+      for (int tt = 0; tt < TT; ++tt) {
+        const uint32_t ka = (bk ^ (16 * k)) + tt * 16 * ROW;  // rows tt*16 + gq and + 8
+        uint32_t c0, c1;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(ka) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(ka + 8 * ROW) : "memory");
+        uint32_t a[4];
+        a[0] = prmt(c0, 0u, 0x4140);
+        a[1] = prmt(c1, 0u, 0x4140);
+        a[2] = prmt(c0, 0u, 0x4342);
+        a[3] = prmt(c1, 0u, 0x4342);
+        mma_f16_16816(sh_[tt], a, bh0, bh1);
+        mma_f16_16816(sl_[tt], a, bl0, bl1);
+      }
+    };
     float bias = 0.0f;
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const int4 z = lds_i4((bq ^ (16 * (k >> 1))) + PG::kOffKz + 128 * (k >> 1) + 64 * ((k & 1) ^ 1));
+    for (int k = 0; k < KH; ++k) {
+      const int4 z = lds_i4(((bq ^ (16 * (k >> 1))) ^ hx) + hoff + PG::kOffKz + 128 * (k >> 1) + 64 * ((k & 1) ^ 1));
       const float w0 = w[4 * k] * f, w1 = w[4 * k + 1] * f, w2 = w[4 * k + 2] * f, w3 = w[4 * k + 3] * f;
       bias = fmaf(w0, (float)z.x, bias);
       bias = fmaf(w1, (float)z.y, bias);
@@ -872,21 +901,12 @@ struct MmaConsumerU8 {
       const uint32_t bh0 = pack_f16(w0, w1), bh1 = pack_f16(w2, w3);
       const float2 h01 = unpack_f16(bh0), h23 = unpack_f16(bh1);
       const uint32_t bl0 = pack_f16(w0 - h01.x, w1 - h01.y), bl1 = pack_f16(w2 - h23.x, w3 - h23.y);
-#pragma unroll
-      for (int tt = 0; tt < TT; ++tt) {
-        const uint32_t ka = (bk ^ (16 * k)) + tt * 16 * ROW;  // rows tt*16 + gq and + 8
-        uint32_t c0, c1;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(ka) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(ka + 8 * ROW) : "memory");
-        uint32_t a[4];
-        a[0] = bytes_to_f16x2(c0, 0x4140);
-        a[1] = bytes_to_f16x2(c1, 0x4140);
-        a[2] = bytes_to_f16x2(c0, 0x4342);
-        a[3] = bytes_to_f16x2(c1, 0x4342);
-        mma_f16_16816(sh_[tt], a, bh0, bh1);
-        mma_f16_16816(sl_[tt], a, bl0, bl1);
-      }
+      qk(k, bh0, bh1, bl0, bl1);
+      if constexpr (kSplit)  // k-step k + 4, prepared by the lane 16 apart
+        qk(k + KH, __shfl_xor_sync(0xffffffffu, bh0, 16), __shfl_xor_sync(0xffffffffu, bh1, 16),
+           __shfl_xor_sync(0xffffffffu, bl0, 16), __shfl_xor_sync(0xffffffffu, bl1, 16));
     }
+    if constexpr (kSplit) bias += __shfl_xor_sync(0xffffffffu, bias, 16);
     bias += __shfl_xor_sync(0xffffffffu, bias, 1);
     bias += __shfl_xor_sync(0xffffffffu, bias, 2);
     // heads 2q, 2q+1 of the score fragments: bias and scale from their lanes
@@ -908,10 +928,10 @@ struct MmaConsumerU8 {
     for (int tt = 0; tt < TT; ++tt) {
       const bool v0 = tt * 16 + gq < lim_a, v1 = tt * 16 + gq + 8 < lim_a;
       const bool w0 = tt * 16 + gq < lim_b, w1 = tt * 16 + gq + 8 < lim_b;
-      s[tt][0] = v0 ? (s[tt][0] - bias0) * mul0 : -INFINITY;
-      s[tt][1] = w0 ? (s[tt][1] - bias1) * mul1 : -INFINITY;
-      s[tt][2] = v1 ? (s[tt][2] - bias0) * mul0 : -INFINITY;
-      s[tt][3] = w1 ? (s[tt][3] - bias1) * mul1 : -INFINITY;
+      s[tt][0] = v0 ? fmaf(s[tt][0], 0x1p24f, -bias0) * mul0 : -INFINITY;
+      s[tt][1] = w0 ? fmaf(s[tt][1], 0x1p24f, -bias1) * mul1 : -INFINITY;
+      s[tt][2] = v1 ? fmaf(s[tt][2], 0x1p24f, -bias0) * mul0 : -INFINITY;
+      s[tt][3] = w1 ? fmaf(s[tt][3], 0x1p24f, -bias1) * mul1 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
       mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
     }
@@ -952,7 +972,11 @@ struct MmaConsumerU8 {
       sum1 += __shfl_xor_sync(0xffffffffu, sum1, off);
     }
     // ---- raw[c][h] = sum_t code_tc p_th; codes past the sequence end are
-    // finite integers met by p = 0, so they add nothing
+    // finite integers met by p = 0, so they add nothing. The codes are f16
+    // subnormals (code * 2^-24) here too: o accumulates in units of 2^-24
+    // (zp sum_p scaled to match) and is scaled back when deposited.
+    sum0 *= 0x1p-24f;
+    sum1 *= 0x1p-24f;
 #pragma unroll
     for (int pr = 0; pr < 4; ++pr) {
       float raw0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, raw1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -967,22 +991,21 @@ struct MmaConsumerU8 {
         const uint32_t u01 = prmt(W0, W1, 0x5140), u23 = prmt(W0, W1, 0x7362);
         const uint32_t v01 = prmt(W2, W3, 0x5140), v23 = prmt(W2, W3, 0x7362);
         uint32_t A0[4], A1[4];
-        A0[0] = bytes_to_f16x2(u01, 0x4140);  // channel +0, tokens t0 t1
-        A0[1] = bytes_to_f16x2(u01, 0x4342);  // channel +1
-        A0[2] = bytes_to_f16x2(v01, 0x4140);  // channel +0, tokens t2 t3
-        A0[3] = bytes_to_f16x2(v01, 0x4342);
-        A1[0] = bytes_to_f16x2(u23, 0x4140);  // channel +2
-        A1[1] = bytes_to_f16x2(u23, 0x4342);  // channel +3
-        A1[2] = bytes_to_f16x2(v23, 0x4140);
-        A1[3] = bytes_to_f16x2(v23, 0x4342);
+        A0[0] = prmt(u01, 0u, 0x4140);  // channel +0, tokens t0 t1
+        A0[1] = prmt(u01, 0u, 0x4342);  // channel +1
+        A0[2] = prmt(v01, 0u, 0x4140);  // channel +0, tokens t2 t3
+        A0[3] = prmt(v01, 0u, 0x4342);
+        A1[0] = prmt(u23, 0u, 0x4140);  // channel +2
+        A1[1] = prmt(u23, 0u, 0x4342);  // channel +3
+        A1[2] = prmt(v23, 0u, 0x4140);
+        A1[3] = prmt(v23, 0u, 0x4342);
         mma_f16_16816(raw0, A0, ph[tt][0], ph[tt][1]);
         mma_f16_16816(raw0, A0, pl[tt][0], pl[tt][1]);
         mma_f16_16816(raw1, A1, ph[tt][0], ph[tt][1]);
         mma_f16_16816(raw1, A1, pl[tt][0], pl[tt][1]);
       }
       // fold: o = alpha o + scale (raw - zp * sum_p)
-      const int c0 = 32 * pr + 4 * gq;
-      const float4 sc = lds_f4((bg ^ (16 * pr)) + PG::kOffVs + 128 * pr);   // channels c0 .. c0 + 3
+      const float4 sc = lds_f4((bg ^ (16 * pr)) + PG::kOffVs + 128 * pr);  // channels 32pr + 4gq .. + 3
       const int4 z = lds_i4((bg ^ (16 * (4 ^ pr))) + PG::kOffVz + 128 * pr);
       float* oa = o[2 * pr];
       float* ob = o[2 * pr + 1];
@@ -1023,13 +1046,13 @@ struct MmaConsumerU8 {
       for (int sd = 0; sd < 2; ++sd) {
         const int c = 32 * pr + 4 * gq + 2 * sd;
         const float* ot = o[2 * pr + sd];
-        if (h0 < G) {
-          st_acc[h0 * D + stash_col<2>(h0, c)] = ot[0];
-          st_acc[h0 * D + stash_col<2>(h0, c + 1)] = ot[2];
+        if (h0 < G) {  // o is held in units of 2^-24
+          st_acc[h0 * D + stash_col<2>(h0, c)] = ot[0] * 0x1p24f;
+          st_acc[h0 * D + stash_col<2>(h0, c + 1)] = ot[2] * 0x1p24f;
         }
         if (h0 + 1 < G) {
-          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c)] = ot[1];
-          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c + 1)] = ot[3];
+          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c)] = ot[1] * 0x1p24f;
+          st_acc[(h0 + 1) * D + stash_col<2>(h0 + 1, c + 1)] = ot[3] * 0x1p24f;
         }
       }
     }
@@ -1066,18 +1089,24 @@ struct MmaConsumerFp8 {
   static_assert(G <= 8, "head group");
   using PG = PageGeom<PA_KV_FP8, 128, BS>;
 
-  uint32_t qp[16];  // q[head g] as bf16 pairs: channels 16k + 4q + {0,1} at 2k, {2,3} at 2k+1
+  // Groups of up to 4 heads (one query token) split the per-page q*scale work
+  // as in the uint8 consumer: lanes 16-31 prepare k-steps 4-7 of heads 0-3.
+  static constexpr bool kSplit = G <= 4;
+  static constexpr int KH = kSplit ? KS / 2 : KS;  // k-steps of q*scale a lane prepares
+  uint32_t qp[2 * KH];  // q[head] as bf16 pairs: channels 16k + 4q + {0,1} at 2k, {2,3} at 2k+1
   float o[8][4];    // O^T tile mt = 2p + s: rows -> channels 32p + 4g + 2s + {0, 1}
   float m0, m1, l0, l1;
   float scale_log2;
 
   __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
     const int lane = threadIdx.x & 31;
-    const int hg = lane >> 2, q4 = (lane & 3) * 4;
+    const int q4 = (lane & 3) * 4;
+    const int hg = kSplit ? (lane >> 2) & 3 : lane >> 2;
+    const int k0 = kSplit ? KH * (lane >> 4) : 0;
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
+    for (int k = 0; k < KH; ++k) {
       uint2 w = make_uint2(0, 0);
-      if (hg < g) w = *reinterpret_cast<const uint2*>(q_smem + hg * D + 16 * k + q4);
+      if (hg < g) w = *reinterpret_cast<const uint2*>(q_smem + hg * D + 16 * (k0 + k) + q4);
       qp[2 * k] = w.x;
       qp[2 * k + 1] = w.y;
     }
@@ -1112,12 +1141,15 @@ struct MmaConsumerFp8 {
     const uint32_t bk = sb + 144 * gq + 4 * q;       // K codes, row gq
     const uint32_t bv = sb + PG::kOffV + 288 * q + 16 * (gq >> 2) + 4 * (gq & 3);  // V codes, row 2q
 
-    // ---- w = q * scale of head gq and its largest magnitude
-    float w[32];
+    // ---- w = q * scale of this lane's head (its KH k-steps) and the head's
+    // largest magnitude
+    static_assert(!(kSplit && MQ), "several query tokens use groups of 8 columns");
+    const uint32_t hx = kSplit ? 32u * (lane >> 4) : 0u, hoff = 8u * hx;  // k-steps 4-7: row phase + 2 rows
+    float w[4 * KH];
     float amax = 0.0f;
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const float4 sc = lds_f4((bq ^ (16 * (k >> 1))) + PG::kOffKs + 128 * (k >> 1) + 64 * (k & 1));
+    for (int k = 0; k < KH; ++k) {
+      const float4 sc = lds_f4(((bq ^ (16 * (k >> 1))) ^ hx) + hoff + PG::kOffKs + 128 * (k >> 1) + 64 * (k & 1));
       w[4 * k + 0] = bf16_lo(qp[2 * k]) * sc.x;
       w[4 * k + 1] = bf16_hi(qp[2 * k]) * sc.y;
       w[4 * k + 2] = bf16_lo(qp[2 * k + 1]) * sc.z;
@@ -1127,6 +1159,7 @@ struct MmaConsumerFp8 {
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if constexpr (kSplit) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
     int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
     ex = ex < 1 ? 1 : ex;
     int sh = 140 - ex;  // 2^sh * amax lands in [2^13, 2^14)
@@ -1141,12 +1174,7 @@ struct MmaConsumerFp8 {
     for (int tt = 0; tt < TT; ++tt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) sh_[tt][i] = sl_[tt][i] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const float w0 = w[4 * k] * f, w1 = w[4 * k + 1] * f, w2 = w[4 * k + 2] * f, w3 = w[4 * k + 3] * f;
-      const uint32_t bh0 = pack_f16(w0, w1), bh1 = pack_f16(w2, w3);
-      const float2 h01 = unpack_f16(bh0), h23 = unpack_f16(bh1);
-      const uint32_t bl0 = pack_f16(w0 - h01.x, w1 - h01.y), bl1 = pack_f16(w2 - h23.x, w3 - h23.y);
+    auto qk = [&](int k, uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
 #pragma unroll
       for (int tt = 0; tt < TT; ++tt) {
         const uint32_t ka = (bk ^ (16 * k)) + tt * 16 * ROW;  // rows tt*16 + gq and + 8
@@ -1161,6 +1189,17 @@ struct MmaConsumerFp8 {
         mma_f16_16816(sh_[tt], a, bh0, bh1);
         mma_f16_16816(sl_[tt], a, bl0, bl1);
       }
+    };
+#pragma unroll
+    for (int k = 0; k < KH; ++k) {
+      const float w0 = w[4 * k] * f, w1 = w[4 * k + 1] * f, w2 = w[4 * k + 2] * f, w3 = w[4 * k + 3] * f;
+      const uint32_t bh0 = pack_f16(w0, w1), bh1 = pack_f16(w2, w3);
+      const float2 h01 = unpack_f16(bh0), h23 = unpack_f16(bh1);
+      const uint32_t bl0 = pack_f16(w0 - h01.x, w1 - h01.y), bl1 = pack_f16(w2 - h23.x, w3 - h23.y);
+      qk(k, bh0, bh1, bl0, bl1);
+      if constexpr (kSplit)  // k-step k + 4, prepared by the lane 16 apart
+        qk(k + KH, __shfl_xor_sync(0xffffffffu, bh0, 16), __shfl_xor_sync(0xffffffffu, bh1, 16),
+           __shfl_xor_sync(0xffffffffu, bl0, 16), __shfl_xor_sync(0xffffffffu, bl1, 16));
     }
     // heads 2q, 2q+1 of the score fragments: the scale from their lanes
     const float mul0 = __shfl_sync(0xffffffffu, finv, 8 * q) * scale_log2;
@@ -1329,7 +1368,12 @@ struct MmaConsumerU4 {
   static_assert(G <= 8, "head group");
   using PG = PageGeom<PA_KV_UINT4, 128, BS>;
 
-  uint32_t qp[16];  // q[head g] bf16 pairs, channels 32k + 8q + {0,1},{2,3},{4,5},{6,7} at 4k..4k+3
+  // Groups of up to 4 heads (one query token) split the per-page q*scale work:
+  // lanes 16-31 prepare k-steps 2 and 3 of heads 0-3 and hand them to lanes
+  // 0-15 by shuffle; the mma's columns 4-7 then hold values no one stores.
+  static constexpr bool kSplit = G <= 4;
+  static constexpr int KH = kSplit ? 2 : 4;  // k-steps of q*scale a lane prepares
+  uint32_t qp[4 * KH];  // q[head] bf16 pairs, channels 32k + 8q + {0,1},{2,3},{4,5},{6,7} at 4k..4k+3
   float o[8][4];    // O^T tile mt = 4o + s: rows -> channels 64o + 8g + 2s + {0, 1}
   float m0, m1, l0, l1;
   float scale_log2;
@@ -1356,11 +1400,14 @@ struct MmaConsumerU4 {
 
   __device__ __forceinline__ void begin_unit(const uint16_t* q_smem, int g, float sl2) {
     const int lane = threadIdx.x & 31;
-    const int hg = lane >> 2, q8 = (lane & 3) * 8;
+    const int q8 = (lane & 3) * 8;
+    // groups of up to 4 heads: lanes 16-31 hold k-steps 2, 3 of heads 0-3
+    const int hg = kSplit ? (lane >> 2) & 3 : lane >> 2;
+    const int k0 = kSplit ? 2 * (lane >> 4) : 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < KH; ++k) {
       uint4 w = make_uint4(0, 0, 0, 0);
-      if (hg < g) w = *reinterpret_cast<const uint4*>(q_smem + hg * D + 32 * k + q8);
+      if (hg < g) w = *reinterpret_cast<const uint4*>(q_smem + hg * D + 32 * (k0 + k) + q8);
       qp[4 * k] = w.x;
       qp[4 * k + 1] = w.y;
       qp[4 * k + 2] = w.z;
@@ -1392,12 +1439,15 @@ struct MmaConsumerU4 {
     const uint32_t bvc = sb + PG::kOffV + 128 * q + 16 * ((gq >> 2) ^ q) + 4 * (gq & 3);  // V codes, row 2q
     const uint32_t bvm = sb + 128 * (gq >> 2) + 32 * (gq & 3) + 16 * (gq >> 2);  // V scales / zero points
 
-    // ---- w = q * scale of head gq (channels 32k + 8q + j) and its largest magnitude
-    float w[32];
+    // ---- w = q * scale of this lane's head (channels 32k + 8q + j of its KH
+    // k-steps) and the head's largest magnitude
+    static_assert(!(kSplit && MQ), "several query tokens use groups of 8 columns");
+    const uint32_t hx = kSplit ? 32u * (lane >> 4) : 0u, hoff = 8u * hx;  // k-steps 2, 3: row phase + 2 rows
+    float w[8 * KH];
     float amax = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t ks = (bq ^ (32 * (k >> 1))) + PG::kOffKs + 128 * k;
+    for (int k = 0; k < KH; ++k) {
+      const uint32_t ks = ((bq ^ (32 * (k >> 1))) ^ hx) + hoff + PG::kOffKs + 128 * k;
       const float4 s0 = lds_f4(ks + 16 * (k & 1));
       const float4 s1 = lds_f4(ks + 16 * ((k & 1) ^ 1));
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -1410,6 +1460,7 @@ struct MmaConsumerU4 {
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if constexpr (kSplit) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
     int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
     ex = ex < 1 ? 1 : ex;
     int sh = 140 - ex;
@@ -1417,55 +1468,79 @@ struct MmaConsumerU4 {
     const float f = __uint_as_float((uint32_t)(127 + sh) << 23);
     const float finv = __uint_as_float((uint32_t)(127 - sh) << 23);
 
+    // Codes enter the mma as f16 subnormals: masking a nibble into a half's low
+    // mantissa bits, exponent zero, gives code * 2^-24 (bits 0-3) or code * 2^-20
+    // (bits 4-7) exactly, with no conversion. The 2^-20 channels (odd j) take
+    // q*scale*f / 16, so every product is code * q*scale*f * 2^-24; the 2^24
+    // comes back in the score below. Channel pairs per k-step: (j0, j4) | (j1, j5),
+    // then (j2, j6) | (j3, j7), as the masks of a code word and of its 8-bit shift
+    // deliver them.
+    const float f16th = f * 0.0625f;
     float sh_[TT][4], sl_[TT][4];
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) sh_[tt][i] = sl_[tt][i] = 0.0f;
-    float bias = 0.0f;
+    // scores += codes of k-step k (rows tt*16 + gq, + 8) x (high, remainder) of q*scale*f
+    auto qk = [&](int k, const uint32_t (&bh)[2][2], const uint32_t (&bl)[2][2]) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t kz = (bq ^ (32 * (k >> 1)) ^ 64) + PG::kOffKz + 128 * k;
+      for (int tt = 0; tt < TT; ++tt) {
+        const uint32_t ka = (bkc ^ (16 * k)) + tt * 16 * ROWB;
+        const uint32_t c0 = lds_u32(ka);
+        const uint32_t c1 = lds_u32((ka ^ 64) + 8 * ROWB);
+        const uint32_t d0 = c0 >> 8, d1 = c1 >> 8;
+        uint32_t a[4] = {c0 & 0x000F000Fu, c1 & 0x000F000Fu, c0 & 0x00F000F0u, c1 & 0x00F000F0u};
+        mma_f16_16816(sh_[tt], a, bh[0][0], bh[0][1]);
+        mma_f16_16816(sl_[tt], a, bl[0][0], bl[0][1]);
+        a[0] = d0 & 0x000F000Fu;
+        a[1] = d1 & 0x000F000Fu;
+        a[2] = d0 & 0x00F000F0u;
+        a[3] = d1 & 0x00F000F0u;
+        mma_f16_16816(sh_[tt], a, bh[1][0], bh[1][1]);
+        mma_f16_16816(sl_[tt], a, bl[1][0], bl[1][1]);
+      }
+    };
+    float bias_e = 0.0f, bias_o = 0.0f;  // sum of q*scale*f*zp over even / odd j (odd: / 16)
+#pragma unroll
+    for (int k = 0; k < KH; ++k) {
+      const uint32_t kz = ((bq ^ (32 * (k >> 1)) ^ 64) ^ hx) + hoff + PG::kOffKz + 128 * k;
       const int4 z0 = lds_i4(kz + 16 * (k & 1));
       const int4 z1 = lds_i4(kz + 16 * ((k & 1) ^ 1));
       const int zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
       float ws[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        ws[j] = w[8 * k + j] * f;
-        bias = fmaf(ws[j], (float)zz[j], bias);
+        ws[j] = w[8 * k + j] * ((j & 1) ? f16th : f);
+        if (j & 1)
+          bias_o = fmaf(ws[j], (float)zz[j], bias_o);
+        else
+          bias_e = fmaf(ws[j], (float)zz[j], bias_e);
       }
-      // k-step 2k: channels +0,+2 | +1,+3 ; k-step 2k+1: +4,+6 | +5,+7
       uint32_t bh[2][2], bl[2][2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int b0 = 4 * h;
-        bh[h][0] = pack_f16(ws[b0], ws[b0 + 2]);
-        bh[h][1] = pack_f16(ws[b0 + 1], ws[b0 + 3]);
+        const int b0 = 2 * h;
+        bh[h][0] = pack_f16(ws[b0], ws[b0 + 4]);
+        bh[h][1] = pack_f16(ws[b0 + 1], ws[b0 + 5]);
         const float2 e0 = unpack_f16(bh[h][0]), e1 = unpack_f16(bh[h][1]);
-        bl[h][0] = pack_f16(ws[b0] - e0.x, ws[b0 + 2] - e0.y);
-        bl[h][1] = pack_f16(ws[b0 + 1] - e1.x, ws[b0 + 3] - e1.y);
+        bl[h][0] = pack_f16(ws[b0] - e0.x, ws[b0 + 4] - e0.y);
+        bl[h][1] = pack_f16(ws[b0 + 1] - e1.x, ws[b0 + 5] - e1.y);
       }
+      qk(k, bh, bl);
+      if constexpr (kSplit) {  // k-step k + 2, prepared by the lane 16 apart
+        uint32_t rh[2][2], rl[2][2];
 #pragma unroll
-      for (int tt = 0; tt < TT; ++tt) {
-        const uint32_t ka = (bkc ^ (16 * k)) + tt * 16 * ROWB;  // rows tt*16 + gq and + 8
-        const uint32_t c0 = lds_u32(ka);
-        const uint32_t c1 = lds_u32((ka ^ 64) + 8 * ROWB);
-        const uint32_t lo0 = c0 & 0x0F0F0F0Fu, hi0 = (c0 >> 4) & 0x0F0F0F0Fu;
-        const uint32_t lo1 = c1 & 0x0F0F0F0Fu, hi1 = (c1 >> 4) & 0x0F0F0F0Fu;
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t sel = h ? 0x4342 : 0x4140;
-          uint32_t a[4];
-          a[0] = bytes_to_f16x2(lo0, sel);
-          a[1] = bytes_to_f16x2(lo1, sel);
-          a[2] = bytes_to_f16x2(hi0, sel);
-          a[3] = bytes_to_f16x2(hi1, sel);
-          mma_f16_16816(sh_[tt], a, bh[h][0], bh[h][1]);
-          mma_f16_16816(sl_[tt], a, bl[h][0], bl[h][1]);
-        }
+          for (int e = 0; e < 2; ++e) {
+            rh[h][e] = __shfl_xor_sync(0xffffffffu, bh[h][e], 16);
+            rl[h][e] = __shfl_xor_sync(0xffffffffu, bl[h][e], 16);
+          }
+        qk(k + 2, rh, rl);
       }
     }
+    float bias = fmaf(16.0f, bias_o, bias_e);
+    if constexpr (kSplit) bias += __shfl_xor_sync(0xffffffffu, bias, 16);
     bias += __shfl_xor_sync(0xffffffffu, bias, 1);
     bias += __shfl_xor_sync(0xffffffffu, bias, 2);
     const float bias0 = __shfl_sync(0xffffffffu, bias, 8 * q);
@@ -1483,10 +1558,10 @@ struct MmaConsumerU4 {
     for (int tt = 0; tt < TT; ++tt) {
       const bool v0 = tt * 16 + gq < lim_a, v1 = tt * 16 + gq + 8 < lim_a;
       const bool w0 = tt * 16 + gq < lim_b, w1 = tt * 16 + gq + 8 < lim_b;
-      s[tt][0] = v0 ? (sh_[tt][0] + sl_[tt][0] - bias0) * mul0 : -INFINITY;
-      s[tt][1] = w0 ? (sh_[tt][1] + sl_[tt][1] - bias1) * mul1 : -INFINITY;
-      s[tt][2] = v1 ? (sh_[tt][2] + sl_[tt][2] - bias0) * mul0 : -INFINITY;
-      s[tt][3] = w1 ? (sh_[tt][3] + sl_[tt][3] - bias1) * mul1 : -INFINITY;
+      s[tt][0] = v0 ? fmaf(sh_[tt][0] + sl_[tt][0], 0x1p24f, -bias0) * mul0 : -INFINITY;
+      s[tt][1] = w0 ? fmaf(sh_[tt][1] + sl_[tt][1], 0x1p24f, -bias1) * mul1 : -INFINITY;
+      s[tt][2] = v1 ? fmaf(sh_[tt][2] + sl_[tt][2], 0x1p24f, -bias0) * mul0 : -INFINITY;
+      s[tt][3] = w1 ? fmaf(sh_[tt][3] + sl_[tt][3], 0x1p24f, -bias1) * mul1 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[tt][0], s[tt][2]));
       mx1 = fmaxf(mx1, fmaxf(s[tt][1], s[tt][3]));
     }
@@ -1526,6 +1601,13 @@ struct MmaConsumerU4 {
       sum1 += __shfl_xor_sync(0xffffffffu, sum1, off);
     }
     // ---- raw[c][h] = sum_t code_tc p_th, then o = alpha o + scale (raw - zp sum_p)
+    // Byte sd of a token's word holds channels 2sd (low nibble: mma row gq) and
+    // 2sd + 1 (high: row gq + 8); one byte permute puts two tokens' bytes in the
+    // two halves, and the masks make them f16 subnormals code * 2^-24 (even
+    // channel) or code * 2^-20 (odd). The rows of o therefore accumulate in those
+    // units (zp sum_p scaled to match) and are scaled back when deposited.
+    const float sum0e = sum0 * 0x1p-24f, sum1e = sum1 * 0x1p-24f;
+    const float sum0o = sum0 * 0x1p-20f, sum1o = sum1 * 0x1p-20f;
 #pragma unroll
     for (int oc = 0; oc < 2; ++oc) {
       float raw[4][4];
@@ -1540,21 +1622,11 @@ struct MmaConsumerU4 {
         const uint32_t W1 = lds_u32(va ^ 64);
         const uint32_t W2 = lds_u32((va ^ 64) + 8 * ROWB);
         const uint32_t W3 = lds_u32(va + 8 * ROWB);
-        const uint32_t l0w = W0 & 0x0F0F0F0Fu, l1w = W1 & 0x0F0F0F0Fu, l2w = W2 & 0x0F0F0F0Fu, l3w = W3 & 0x0F0F0F0Fu;
-        const uint32_t h0w = (W0 >> 4) & 0x0F0F0F0Fu, h1w = (W1 >> 4) & 0x0F0F0F0Fu;
-        const uint32_t h2w = (W2 >> 4) & 0x0F0F0F0Fu, h3w = (W3 >> 4) & 0x0F0F0F0Fu;
-        const uint32_t x01 = prmt(l0w, l1w, 0x5140), x23 = prmt(l0w, l1w, 0x7362);  // even ch, t0 t1
-        const uint32_t y01 = prmt(h0w, h1w, 0x5140), y23 = prmt(h0w, h1w, 0x7362);  // odd ch, t0 t1
-        const uint32_t z01 = prmt(l2w, l3w, 0x5140), z23 = prmt(l2w, l3w, 0x7362);  // even ch, t2 t3
-        const uint32_t u01 = prmt(h2w, h3w, 0x5140), u23 = prmt(h2w, h3w, 0x7362);  // odd ch, t2 t3
 #pragma unroll
         for (int sd = 0; sd < 4; ++sd) {
-          const uint32_t sel = (sd & 1) ? 0x4342 : 0x4140;
-          uint32_t A[4];
-          A[0] = bytes_to_f16x2(sd < 2 ? x01 : x23, sel);
-          A[1] = bytes_to_f16x2(sd < 2 ? y01 : y23, sel);
-          A[2] = bytes_to_f16x2(sd < 2 ? z01 : z23, sel);
-          A[3] = bytes_to_f16x2(sd < 2 ? u01 : u23, sel);
+          const uint32_t sel = (uint32_t)(sd | (sd << 4) | ((4 + sd) << 8) | ((4 + sd) << 12));
+          const uint32_t x01 = prmt(W0, W1, sel), x89 = prmt(W2, W3, sel);
+          uint32_t A[4] = {x01 & 0x000F000Fu, x01 & 0x00F000F0u, x89 & 0x000F000Fu, x89 & 0x00F000F0u};
           mma_f16_16816(raw[sd], A, ph[tt][0], ph[tt][1]);
           mma_f16_16816(raw[sd], A, pl[tt][0], pl[tt][1]);
         }
@@ -1570,10 +1642,10 @@ struct MmaConsumerU4 {
       for (int sd = 0; sd < 4; ++sd) {
         float* ot = o[4 * oc + sd];
         const int ce = 2 * sd, co = 2 * sd + 1;  // channels of rows g and g+8
-        ot[0] = fmaf(a0, ot[0], sc[ce] * fmaf(-zf[ce], sum0, raw[sd][0]));
-        ot[1] = fmaf(a1, ot[1], sc[ce] * fmaf(-zf[ce], sum1, raw[sd][1]));
-        ot[2] = fmaf(a0, ot[2], sc[co] * fmaf(-zf[co], sum0, raw[sd][2]));
-        ot[3] = fmaf(a1, ot[3], sc[co] * fmaf(-zf[co], sum1, raw[sd][3]));
+        ot[0] = fmaf(a0, ot[0], sc[ce] * fmaf(-zf[ce], sum0e, raw[sd][0]));
+        ot[1] = fmaf(a1, ot[1], sc[ce] * fmaf(-zf[ce], sum1e, raw[sd][1]));
+        ot[2] = fmaf(a0, ot[2], sc[co] * fmaf(-zf[co], sum0o, raw[sd][2]));
+        ot[3] = fmaf(a1, ot[3], sc[co] * fmaf(-zf[co], sum1o, raw[sd][3]));
       }
     }
   }
@@ -1604,13 +1676,13 @@ struct MmaConsumerU4 {
       for (int sd = 0; sd < 4; ++sd) {
         const int c = 64 * oc + 8 * gq + 2 * sd;
         const float* ot = o[4 * oc + sd];
-        if (h0 < G) {
-          st_acc[h0 * D + stash_col<3>(h0, c)] = ot[0];
-          st_acc[h0 * D + stash_col<3>(h0, c + 1)] = ot[2];
+        if (h0 < G) {  // even channels in units of 2^-24, odd ones of 2^-20
+          st_acc[h0 * D + stash_col<3>(h0, c)] = ot[0] * 0x1p24f;
+          st_acc[h0 * D + stash_col<3>(h0, c + 1)] = ot[2] * 0x1p20f;
         }
         if (h0 + 1 < G) {
-          st_acc[(h0 + 1) * D + stash_col<3>(h0 + 1, c)] = ot[1];
-          st_acc[(h0 + 1) * D + stash_col<3>(h0 + 1, c + 1)] = ot[3];
+          st_acc[(h0 + 1) * D + stash_col<3>(h0 + 1, c)] = ot[1] * 0x1p24f;
+          st_acc[(h0 + 1) * D + stash_col<3>(h0 + 1, c + 1)] = ot[3] * 0x1p20f;
         }
       }
     }
