@@ -264,6 +264,15 @@ __device__ __forceinline__ uint32_t bytes_to_f16x2(uint32_t w, uint32_t sel) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x by the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, a subnormal result flushes to zero, 2^-inf = 0), for the
+// per-page softmax weights whose f16 high + remainder split keeps 22 bits.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -52,7 +52,10 @@ namespace {
 // and run eight.
 template <int KV, bool TC, int BS>
 constexpr int consumer_warps() {
-  return !TC ? 8 : (KV == PA_KV_BF16 ? 4 : 8);
+  // Quantised tensor-core kernels run one block of 168-register threads per SM;
+  // 12 warps (3 per sub-partition) still fit that budget. uint4 keeps 8: its
+  // 6 KB pages give it 24 ring stages with 8 warps against 20 with 10.
+  return !TC ? 8 : (KV == PA_KV_BF16 ? 4 : (KV == PA_KV_UINT4 ? 8 : 10));
 }
 constexpr int kMaxSegs = 64;         // segments per window
 constexpr int kMaxWinPages = 1024;   // pages per window (block-table entries staged in smem)
@@ -644,15 +647,15 @@ struct MmaConsumerBf16 {
     // a column that has seen no token yet (several query tokens per
     // sequence) keeps an empty state instead of forming inf - inf
     const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
-    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
+    const float a0 = ex2_approx(m0 - r0), a1 = ex2_approx(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
-      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
+      const float p0 = ex2_approx(s[tt][0] - r0), p1 = ex2_approx(s[tt][1] - r1);
+      const float p2 = ex2_approx(s[tt][2] - r0), p3 = ex2_approx(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
@@ -944,15 +947,15 @@ struct MmaConsumerU8 {
     // a column that has seen no token yet (several query tokens per
     // sequence) keeps an empty state instead of forming inf - inf
     const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
-    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
+    const float a0 = ex2_approx(m0 - r0), a1 = ex2_approx(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
-      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
+      const float p0 = ex2_approx(s[tt][0] - r0), p1 = ex2_approx(s[tt][1] - r1);
+      const float p2 = ex2_approx(s[tt][2] - r0), p3 = ex2_approx(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
@@ -1230,15 +1233,15 @@ struct MmaConsumerFp8 {
     // a column that has seen no token yet (several query tokens per
     // sequence) keeps an empty state instead of forming inf - inf
     const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
-    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
+    const float a0 = ex2_approx(m0 - r0), a1 = ex2_approx(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
-      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
+      const float p0 = ex2_approx(s[tt][0] - r0), p1 = ex2_approx(s[tt][1] - r1);
+      const float p2 = ex2_approx(s[tt][2] - r0), p3 = ex2_approx(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);
@@ -1574,15 +1577,15 @@ struct MmaConsumerU4 {
     // a column that has seen no token yet (several query tokens per
     // sequence) keeps an empty state instead of forming inf - inf
     const float r0 = MQ && n0 == -INFINITY ? 0.0f : n0, r1 = MQ && n1 == -INFINITY ? 0.0f : n1;
-    const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
+    const float a0 = ex2_approx(m0 - r0), a1 = ex2_approx(m1 - r1);
     m0 = n0;
     m1 = n1;
     uint32_t ph[TT][2], pl[TT][2];
     float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
     for (int tt = 0; tt < TT; ++tt) {
-      const float p0 = exp2f(s[tt][0] - r0), p1 = exp2f(s[tt][1] - r1);
-      const float p2 = exp2f(s[tt][2] - r0), p3 = exp2f(s[tt][3] - r1);
+      const float p0 = ex2_approx(s[tt][0] - r0), p1 = ex2_approx(s[tt][1] - r1);
+      const float p2 = ex2_approx(s[tt][2] - r0), p3 = ex2_approx(s[tt][3] - r1);
       ps0 += p0 + p2;
       ps1 += p1 + p3;
       const uint32_t h01 = pack_f16(p0, p1), h23 = pack_f16(p2, p3);

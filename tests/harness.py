@@ -111,7 +111,8 @@ def gpu_decode(gpool, wl, num_splits=0, out_fill=float("nan"), path="auto", comb
 
 def check_attention(got, ref, what=""):
     got = np.asarray(got, np.float64)
-    assert np.isfinite(got).all(), f"{what}: non-finite outputs"
+    bad_rows = np.where(~np.isfinite(got).all(axis=1))[0]
+    assert bad_rows.size == 0, f"{what}: non-finite outputs in rows {bad_rows[:16].tolist()} of {got.shape[0]}"
     err = np.abs(got - ref)
     max_abs = float(err.max()) if err.size else 0.0
     row_rel = err.max(axis=1) / np.maximum(np.abs(ref).max(axis=1), 1e-6) if err.size else np.zeros(1)
