@@ -53,8 +53,8 @@ namespace {
 template <int KV, bool TC, int BS>
 constexpr int consumer_warps() {
   // Quantised tensor-core kernels run one block of 168-register threads per SM;
-  // 12 warps (3 per sub-partition) still fit that budget. uint4 keeps 8: its
-  // 6 KB pages give it 24 ring stages with 8 warps against 20 with 10.
+  // 12 warps (3 per sub-partition) still fit that budget. uint4 pages (32
+  // tokens) measured faster with 8.
   return !TC ? 8 : (KV == PA_KV_BF16 ? 4 : (KV == PA_KV_UINT4 ? 8 : 10));
 }
 constexpr int kMaxSegs = 64;         // segments per window
@@ -1898,10 +1898,11 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   // belong to the same consumer warp: a warp then starts waiting for a fill
   // only after it has itself released the fill before, and its parity wait
   // can never mistake an older phase still in flight for the one it wants.
-  // (NST is a multiple of kConsumerWarps, so the result is at least one warp
-  // count.)
-  const int nst = (int)max((long long)min(NST, kConsumerWarps), min((long long)NST, max(16LL, min(24LL, (small ? (long long)((unsigned)T / (unsigned)Gc) : T / Gc) / 8)))) /
-                  kConsumerWarps * kConsumerWarps;
+  // Rounded up (NST is a multiple of kConsumerWarps, so the result stays
+  // within the ring and is at least one warp count).
+  const int nst = (int)min((long long)NST, (max((long long)min(NST, kConsumerWarps), min((long long)NST, max(16LL, min(24LL, (small ? (long long)((unsigned)T / (unsigned)Gc) : T / Gc) / 8)))) +
+                                            kConsumerWarps - 1) /
+                                               kConsumerWarps * kConsumerWarps);
   // every thread block finds the sequence holding its first page
   if (one_pass) {
     const long long lo = (long long)(my_incl - my_pages) * Hkv, hi = (long long)my_incl * Hkv;
