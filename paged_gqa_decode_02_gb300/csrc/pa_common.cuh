@@ -286,9 +286,18 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t w) {
 // largest finite 448) through the hardware conversions. Every E4M3 value is
 // an f16 value, so widening is exact.
 // Two codes (bits 0-7 and 8-15 of w) -> f16x2 (low half from bits 0-7).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Two E4M3 codes widened exactly to an f16 pair (every E4M3 value is an f16
+// value): the codes in the low (_lo) or high (_hi) 16 bits of w, the lower
+// byte to the lower half. The half is taken as a register view, no shift.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}" : "=r"(d) : "r"(w));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, hi;\n}" : "=r"(d) : "r"(w));
+  return d;
 }
 
 __device__ __forceinline__ float e4m3_to_float(uint32_t code) {

@@ -1185,10 +1185,10 @@ struct MmaConsumerFp8 {
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c0) : "r"(ka) : "memory");
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c1) : "r"(ka + 8 * ROW) : "memory");
         uint32_t a[4];
-        a[0] = e4m3x2_to_f16x2(c0);        // channels 16k + 4q + {0, 1}
-        a[1] = e4m3x2_to_f16x2(c1);
-        a[2] = e4m3x2_to_f16x2(c0 >> 16);  // channels 16k + 4q + {2, 3}
-        a[3] = e4m3x2_to_f16x2(c1 >> 16);
+        a[0] = e4m3x2_lo_to_f16x2(c0);  // channels 16k + 4q + {0, 1}
+        a[1] = e4m3x2_lo_to_f16x2(c1);
+        a[2] = e4m3x2_hi_to_f16x2(c0);  // channels 16k + 4q + {2, 3}
+        a[3] = e4m3x2_hi_to_f16x2(c1);
         mma_f16_16816(sh_[tt], a, bh0, bh1);
         mma_f16_16816(sl_[tt], a, bl0, bl1);
       }
@@ -1276,14 +1276,14 @@ struct MmaConsumerFp8 {
         const uint32_t u01 = prmt(W0, W1, 0x5140), u23 = prmt(W0, W1, 0x7362);
         const uint32_t v01 = prmt(W2, W3, 0x5140), v23 = prmt(W2, W3, 0x7362);
         uint32_t A0[4], A1[4];
-        A0[0] = e4m3x2_to_f16x2(u01);        // channel +0, tokens t0 t1
-        A0[1] = e4m3x2_to_f16x2(u01 >> 16);  // channel +1
-        A0[2] = e4m3x2_to_f16x2(v01);        // channel +0, tokens t2 t3
-        A0[3] = e4m3x2_to_f16x2(v01 >> 16);
-        A1[0] = e4m3x2_to_f16x2(u23);        // channel +2
-        A1[1] = e4m3x2_to_f16x2(u23 >> 16);  // channel +3
-        A1[2] = e4m3x2_to_f16x2(v23);
-        A1[3] = e4m3x2_to_f16x2(v23 >> 16);
+        A0[0] = e4m3x2_lo_to_f16x2(u01);  // channel +0, tokens t0 t1
+        A0[1] = e4m3x2_hi_to_f16x2(u01);  // channel +1
+        A0[2] = e4m3x2_lo_to_f16x2(v01);  // channel +0, tokens t2 t3
+        A0[3] = e4m3x2_hi_to_f16x2(v01);
+        A1[0] = e4m3x2_lo_to_f16x2(u23);  // channel +2
+        A1[1] = e4m3x2_hi_to_f16x2(u23);  // channel +3
+        A1[2] = e4m3x2_lo_to_f16x2(v23);
+        A1[3] = e4m3x2_hi_to_f16x2(v23);
         mma_f16_16816(raw0, A0, ph[tt][0], ph[tt][1]);
         mma_f16_16816(raw0, A0, pl[tt][0], pl[tt][1]);
         mma_f16_16816(raw1, A1, ph[tt][0], ph[tt][1]);
