@@ -273,13 +273,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// lo, hi rounded to nearest-even f16 and packed (lo in the lower half): one cvt
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
+// the two halves of an f16 pair widened exactly to fp32
 __device__ __forceinline__ float2 unpack_f16(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  float2 r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(w));
+  return r;
 }
 
 // E4M3 (OCP 8-bit floating point: bias 7, 3 mantissa bits, no infinities,
