@@ -269,6 +269,13 @@ class WorkloadRun:
         del fills
         step = self.step = wl.step_call(n_q)
         self.st = (self.d(step.k_bits), self.d(step.v_bits), self.d(step.cu_new), self.d(step.ctx_lens))
+        if n_q == 1:  # the same new tokens as rows [B][Hkv][D], for the fused decode step
+            kr = np.zeros((wl.batch, wl.num_kv_heads, wl.head_dim), np.uint16)
+            vr = np.zeros_like(kr)
+            for b in range(wl.batch):
+                if step.cu_new[b + 1] > step.cu_new[b]:
+                    kr[b], vr[b] = step.k_bits[step.cu_new[b]], step.v_bits[step.cu_new[b]]
+            self.rows = (self.d(kr), self.d(vr))
         B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
         self.q_bits = wl.q_bits if n_q == 1 else W.multi_token_queries(100, B, n_q, Hq, D)
         self.table, self.lens, self.q = self.d(wl.block_table), self.d(wl.seq_lens), self.d(self.q_bits)
@@ -301,6 +308,11 @@ class WorkloadRun:
         k, v, cu, ctx = self.st
         self.pools[i].append_kv(k, v, cu, ctx, self.table, max_new_per_seq=self.n_q)
         self.decode_call(i)
+
+    def fused_step_call(self, i):
+        # the decode step in one decode launch (pa_decode_step)
+        self.pools[i].decode_step(self.rows[0], self.rows[1], self.q, self.table, self.lens, self.wl.softmax_scale,
+                                  out=self.outs[i], workspace=self.ws[i], num_splits=self.args.splits)
 
     def isolated(self, fn, K):
         torch = self.torch
@@ -396,6 +408,7 @@ def measure(run, dist, world, K, warmup, peak, peak_kind, K_e2e):
     dec_ms = run.isolated(run.decode_call, K)
     b2b_step = run.back_to_back(run.step_call, K)
     b2b_dec = run.back_to_back(run.decode_call, K)
+    fused_ms = run.isolated(run.fused_step_call, K) if n_q == 1 else None
     st, flags = run.device_error()
     assert st == 0 and flags == 0, f"device error word {flags:#x} during timing ({run.name})"
     t_step = _max_over_ranks(dist, statistics.mean(step_ms) / 1e3)
@@ -426,6 +439,10 @@ def measure(run, dist, world, K, warmup, peak, peak_kind, K_e2e):
                          "decode_gbs": ach_b2b, "decode_frac": ach_b2b / peak, "pool_copies": run.n_rot},
         "e2e": {"value": world * B * n_q / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
+        "fused_step_us": None if fused_ms is None else {
+            "isolated": _max_over_ranks(dist, statistics.mean(fused_ms) / 1e3) * 1e6,
+            "note": "pa_decode_step (store the new tokens and attend in one decode launch + combine), timed "
+                    "like the step above; the step (pa_append_kv then pa_decode) is what value reports"},
         "launch": {"num_splits": run.splits_used, "decode_path": run.args.path,
                    "combine": run.args.combine if n_q == 1 else "separate", "early_plan": not run.args.no_early_plan,
                    "unit_cost": run.args.unit_cost},

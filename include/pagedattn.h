@@ -165,6 +165,28 @@ PA_API pa_status pa_decode(pa_pool* pool, const void* q, const int32_t* block_ta
                     int32_t max_blocks, float softmax_scale, float* out, void* workspace,
                     size_t workspace_bytes, int32_t num_splits, void* stream);
 
+/* pa_decode_step: the decode step in one decode launch (plus the combine):
+ * store every sequence's new token (TFFInfer section 3.8: KV cache store,
+ * then attention) and attend, as pa_append_kv with one token per sequence
+ * (cu_new = 0, 1, ..., batch; ctx_lens = seq_lens - 1) followed by pa_decode
+ * would, with the same codes, scales and zero points bit for bit. The thread
+ * block that reads a sequence's last page for a kv head stores that head's
+ * new token into the block first (re-quantising it for uint8 / uint4 / fp8
+ * pools), so the block is written and read once.
+ *   k_new, v_new device bf16 [batch][Hkv][head_dim]: row b is sequence b's
+ *                new token, at position seq_lens[b] - 1 (ignored when
+ *                seq_lens[b] == 0)
+ *   the other arguments as pa_decode; seq_lens counts the new token.
+ * The blocks receiving new tokens must not be shared with another sequence
+ * (copy-on-write first) and must not be written by a kernel still running;
+ * with PA_DECODE_EARLY_PLAN the preceding kernel must, as for pa_decode, write
+ * neither seq_lens nor block_table. Errors as pa_decode; null k_new / v_new:
+ * PA_ERR_INVALID_ARG (nothing launched). */
+PA_API pa_status pa_decode_step(pa_pool* pool, const void* k_new, const void* v_new, const void* q,
+                                const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                                int32_t num_q_heads, int32_t max_blocks, float softmax_scale, float* out,
+                                void* workspace, size_t workspace_bytes, int32_t num_splits, void* stream);
+
 /* pa_decode_noalloc: pa_decode for callers that cannot allocate device
  * memory (no allocator on the hot path, memory reserved up front, or no
  * allocator to hand a workspace from). The pages this library follows have no

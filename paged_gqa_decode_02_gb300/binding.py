@@ -74,6 +74,7 @@ def lib():
         L.pa_destroy.argtypes = [P]
         L.pa_append_kv.argtypes = [P, P, P, P, P, P, I32, I32, I32, P]
         L.pa_decode.argtypes = [P, P, P, P, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
+        L.pa_decode_step.argtypes = [P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
         L.pa_decode_workspace_bytes.argtypes = [P, I32, I32, I32]
         L.pa_decode_workspace_bytes.restype = SZ
         L.pa_decode_multi.argtypes = [P, P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, P]
@@ -346,6 +347,22 @@ class PagedKVPool:
             workspace = self.workspace(B, Hq, num_splits)
         pa_decode(self.handle, q, block_table, seq_lens, B, Hq, int(block_table.shape[1]),
                   softmax_scale, out, workspace, workspace.numel(), num_splits, stream)
+        return out
+
+    def decode_step(self, k_new, v_new, q, block_table, seq_lens, softmax_scale, out=None, workspace=None,
+                    num_splits=0, stream=None):
+        """The decode step in one launch: store each sequence's new token
+        (k_new / v_new [B, Hkv, D] bf16 bits, position seq_lens[b] - 1) and
+        attend, as append_kv of one token per sequence then decode."""
+        B, Hq, D = q.shape
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device=self.device)
+        if workspace is None:
+            workspace = self.workspace(B, Hq, num_splits)
+        _check(lib().pa_decode_step(self.handle, _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(block_table),
+                                    _ptr(seq_lens), int(B), int(Hq), int(block_table.shape[1]),
+                                    float(softmax_scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
+                                    int(num_splits), _stream(stream)))
         return out
 
     def decode_multi(self, q, block_table, seq_lens, softmax_scale, out=None, num_splits=0, stream=None):

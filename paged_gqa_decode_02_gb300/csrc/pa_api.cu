@@ -414,11 +414,11 @@ size_t pa_decode_workspace_bytes(const pa_pool* p, int32_t batch, int32_t num_q_
   return pa::decode_workspace_bytes(ctas, batch, Hkv, group, p->desc.head_dim);
 }
 
-pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
-                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
-                    int32_t max_blocks, float softmax_scale, float* out, void* workspace,
-                    size_t workspace_bytes, int32_t num_splits, void* stream) {
-  g_last_error[0] = 0;
+// pa_decode, and with k_new / v_new the fused decode step (pa_decode_step).
+static pa_status decode_impl(pa_pool* p, const void* q, const int32_t* block_table, const int32_t* seq_lens,
+                             int32_t batch, int32_t num_q_heads, int32_t max_blocks, float softmax_scale,
+                             float* out, void* workspace, size_t workspace_bytes, int32_t num_splits,
+                             const void* k_new, const void* v_new, void* stream) {
   if (!p) return fail(PA_ERR_INVALID_ARG, "null pool%s");
   if (batch < 0 || max_blocks < 0 || num_splits < 0)
     return fail(PA_ERR_INVALID_ARG, "negative batch, max_blocks or num_splits%s");
@@ -450,10 +450,31 @@ pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
   L.early_plan = p->early_plan;
   L.epoch = next_epoch();
   L.unit_cost = p->unit_cost >= 0 ? p->unit_cost : default_unit_cost(p);
+  L.k_new = k_new;
+  L.v_new = v_new;
   cudaError_t e = pa::launch_decode(p->desc.kv_dtype, p->dev, p->maps, q, block_table, seq_lens, out,
                                     workspace, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_gqa_decode launch");
   return PA_OK;
+}
+
+pa_status pa_decode(pa_pool* p, const void* q, const int32_t* block_table,
+                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                    int32_t max_blocks, float softmax_scale, float* out, void* workspace,
+                    size_t workspace_bytes, int32_t num_splits, void* stream) {
+  g_last_error[0] = 0;
+  return decode_impl(p, q, block_table, seq_lens, batch, num_q_heads, max_blocks, softmax_scale, out, workspace,
+                     workspace_bytes, num_splits, nullptr, nullptr, stream);
+}
+
+pa_status pa_decode_step(pa_pool* p, const void* k_new, const void* v_new, const void* q,
+                         const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                         int32_t num_q_heads, int32_t max_blocks, float softmax_scale, float* out,
+                         void* workspace, size_t workspace_bytes, int32_t num_splits, void* stream) {
+  g_last_error[0] = 0;
+  if (batch > 0 && (!k_new || !v_new)) return fail(PA_ERR_INVALID_ARG, "null k_new or v_new%s");
+  return decode_impl(p, q, block_table, seq_lens, batch, num_q_heads, max_blocks, softmax_scale, out, workspace,
+                     workspace_bytes, num_splits, k_new, v_new, stream);
 }
 
 // Column groups of several query tokens: tokens per group (as many whole

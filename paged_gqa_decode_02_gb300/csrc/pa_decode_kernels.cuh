@@ -41,6 +41,7 @@
 
 #include "pa_common.cuh"
 #include "pa_kernels.h"
+#include "pa_quant.cuh"
 
 namespace pa {
 
@@ -105,9 +106,9 @@ struct Smem {
   using PG = PageGeom<KV, D, BS>;
   static constexpr int kStages = W * NS;
   static constexpr int kQBytes = G * D * 2;
-  // full[kStages], empty[kStages], qfull[2], qempty[2], deposited, merged
+  // full[kStages], empty[kStages], qfull[2], qempty[2], deposited, merged, appended
   static constexpr size_t kOffBars = 0;
-  static constexpr size_t kBarBytes = (2 * kStages + 6) * 8;
+  static constexpr size_t kBarBytes = (2 * kStages + 7) * 8;
   static constexpr size_t kOffFlags = kBarBytes;  // int32 per stage
   static constexpr size_t kOffSegs = (kOffFlags + kStages * 4 + 15) / 16 * 16;
   static constexpr size_t kOffPlan = kOffSegs + kMaxSegs * sizeof(Seg);  // 32 int64
@@ -150,7 +151,39 @@ struct DecodeParams {
   // are [B][n_q][Hq][D]. Single-token kernels: n_q = n_cg = tpg = 1,
   // g_heads = group.
   int n_q, n_cg, tpg, g_heads;
+  // Fused decode step (single-token kernels): each sequence's last token,
+  // row b of k_new / v_new (bf16 [batch][Hkv][D]), is stored into its block
+  // (re-quantising it for quantised pools, as kv_quant_append does) by the
+  // thread block that owns the unit's last page, before that page is read.
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int append;
 };
+
+// The fused decode step's store for one unit: the new token (the last of
+// `len`) of sequence b, kv head h, into its block, the record `page` (the
+// unit's last page), K then V. Called by every consumer thread, kThreads of
+// them (whole warps): lanes of a channel adjacent, channels in passes; warps
+// whose channels are past head_dim sit a pass out. Not inlined: the page loop
+// keeps its registers.
+template <int KV, int BS>
+__device__ __noinline__ void append_unit_tail(const PoolDev& pool, long long page, int b, int h, int len,
+                                              const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
+                                              int ct, int kThreads) {
+  constexpr int TL = tok_lanes<BS>();
+  const int D = pool.head_dim, Hkv = pool.num_kv_heads;
+  const int lane = ct & 31, ts = lane & (TL - 1);
+  const int old_cnt = (len - 1) % BS;                 // stored tokens before the new one
+  const long long row0 = (long long)b - old_cnt;     // k_new row of slot s: row0 + s
+  for (int base = 0; base < D; base += kThreads / TL) {
+    const int c = base + ct / TL;
+    if (base + (ct & ~31) / TL >= D) continue;        // the whole warp is past the last channel
+#pragma unroll
+    for (int is_v = 0; is_v < 2; ++is_v)
+      append_block<KV, BS>(pool, page, is_v, c, ts, lane, old_cnt, old_cnt + 1, is_v ? v_new : k_new, row0,
+                           Hkv, h);
+  }
+}
 
 // ------------------------------------------------------------------ split-KV merge
 //
@@ -1767,7 +1800,10 @@ __device__ __noinline__ void merge_stash_warp(const float* __restrict__ st_acc,
   }
 }
 
-template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ>
+// AP: the fused decode step's instantiation (each unit's new token stored by
+// the block that reads the unit's last page, before that page is read); the
+// plain decode's kernels are compiled without that code.
+template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ, bool AP = false>
 __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     paged_gqa_decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kConsumerWarps = consumer_warps<KV, TC, BS>();
@@ -1794,6 +1830,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   uint64_t* qempty = qfull + 2;
   uint64_t* deposited = qempty + 2;  // every consumer warp has stashed the unit
   uint64_t* merged = deposited + 1;   // the merger has read the stash (free again)
+  uint64_t* appended = merged + 1;    // fused step: this window's new tokens are stored
   int32_t* stage_flag = reinterpret_cast<int32_t*>(smem + SM::kOffFlags);
   Seg* segs = reinterpret_cast<Seg*>(smem + SM::kOffSegs);
   long long* plan = reinterpret_cast<long long*>(smem + SM::kOffPlan);
@@ -1840,6 +1877,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     }
     mbar_init(deposited, kConsumerWarps);
     mbar_init(merged, 1);
+    if constexpr (AP) mbar_init(appended, kConsumerWarps);
     abort_flag = 0;
     q_issued[0] = q_issued[1] = -1;
     fence_mbar_init();
@@ -1987,6 +2025,8 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
   uint64_t pol = policy_evict_first();
   Cons cons;  // consumer warps' online-softmax state; persists across windows
   int n_dep = 0;  // units this warp has deposited (phase of `merged` to wait for)
+  int win = 0;    // windows done (phase of `appended` to wait for)
+  constexpr bool fuse_append = AP && !MQ;  // the fused decode step's kernels only
 
   while (pos < e_i) {
     // ---- build this window's segment list (warp 0)
@@ -2216,6 +2256,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       };
       int qseg = 0;    // segments whose first page the issue has reached
       int q_sent = 0;  // segments whose q has been sent (lane 0's count)
+      bool tails_released = false;  // fused step: the consumers' stores of this window are done
       for (int k = kw0; k < kw1;) {
         if (qseg < nseg && segs[qseg].k0 == k) {
           if (lane == 0 && q_sent == qseg) {
@@ -2230,6 +2271,18 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
         if (lane == 0 && q_sent == qseg && q_sent < nseg && send_q(q_sent, false)) ++q_sent;
         int kend = min(kw1, k + (nst < 32 ? nst : 32));
         if (qseg < nseg) kend = min(kend, segs[qseg].k0);
+        if (fuse_append && !tails_released) {
+          // this sub-batch lies in segment qseg - 1: if it holds that unit's
+          // last page, the consumers must have stored the new token first
+          const Seg& cs = segs[qseg - 1];
+          if (cs.len > 0 && cs.lp0 + cs.npages == (cs.len + BS - 1) / BS && kend == cs.k0 + cs.npages) {
+            if (!abort_flag && !mbar_wait_bounded(appended, win & 1)) {
+              set_error(p.pool.err, PA_DEVERR_TIMEOUT);
+              abort_flag = 1;
+            }
+            tails_released = true;
+          }
+        }
         const int kk = k + lane;
         if (kk < kend) {
           const int rec = phys_s[kk - kw0];  // record index, -1 for a bad table entry
@@ -2273,6 +2326,23 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
       // ---------------------------------------------------------- consumers
       const int cw = warp - 1;
       float* pbuf = pbuf_all + cw * BS * G;
+      if constexpr (fuse_append) {
+        // fused decode step: store the new token of every unit whose last page
+        // lies in this window (this block owns that page), then release the
+        // window's last pages to the producer. The stores go out through the
+        // generic proxy and the pages come in by TMA: fence the two.
+        for (int si = 0; si < nseg; ++si) {
+          const Seg& sg = segs[si];
+          if (sg.len <= 0 || sg.lp0 + sg.npages != (sg.len + BS - 1) / BS) continue;  // not the unit's last page
+          const int rec = phys_s[sg.k0 + sg.npages - 1 - kw0];
+          if (rec >= 0)
+            append_unit_tail<KV, BS>(p.pool, rec, seq_of<MQ>(p, sg.b), sg.h, sg.len, p.k_new, p.v_new,
+                                     cw * 32 + lane, kConsumerWarps * 32);
+        }
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(appended);
+      }
       if (pos == s_i) {
         // warm the instruction cache while the first pages are in flight: the
         // deposit runs once per unit, and its first run would otherwise fetch
@@ -2424,6 +2494,7 @@ __global__ void __launch_bounds__((consumer_warps<KV, TC, BS>() + 2) * 32, 1)
     lens_cached = false;
     pos = wend;
     k_done = kw1;
+    if constexpr (fuse_append) ++win;
     __syncthreads();
   }
   // every issued copy was waited on by a consumer (or the abort path skipped
@@ -2631,10 +2702,10 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
-template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ = false>
+template <int KV, int D, int BS, int G, int NS, bool TC, bool MQ = false, bool AP = false>
 cudaError_t launch_t(const DecodeParams& prm, const DecodeLaunch& L, cudaStream_t stream) {
   using SM = Smem<KV, D, BS, G, NS, consumer_warps<KV, TC, BS>(), TC>;
-  auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC, MQ>;
+  auto kern = paged_gqa_decode_kernel<KV, D, BS, G, NS, TC, MQ, AP>;
   static std::atomic<unsigned long long> ready_dec{0}, ready_comb{0};  // per instantiation, per device
   cudaError_t e = prepare_kernel(kern, (int)SM::kBytes, ready_dec);
   if (e != cudaSuccess) return e;
@@ -2689,6 +2760,11 @@ cudaError_t dispatch_g(const DecodeParams& prm, const DecodeLaunch& L, cudaStrea
   constexpr int W = consumer_warps<KV, TC, BS>();
   // several query tokens per sequence: column groups of up to 8 columns
   if (L.n_q > 1) return launch_t<KV, D, BS, 8, stages_per_warp<KV, D, BS, 8, W, TC>(), TC, true>(prm, L, s);
+  if (prm.append) {  // the fused decode step
+    if (L.group <= 2) return launch_t<KV, D, BS, 2, stages_per_warp<KV, D, BS, 2, W, TC>(), TC, false, true>(prm, L, s);
+    if (L.group <= 4) return launch_t<KV, D, BS, 4, stages_per_warp<KV, D, BS, 4, W, TC>(), TC, false, true>(prm, L, s);
+    return launch_t<KV, D, BS, 8, stages_per_warp<KV, D, BS, 8, W, TC>(), TC, false, true>(prm, L, s);
+  }
   if (L.group <= 2) return launch_t<KV, D, BS, 2, stages_per_warp<KV, D, BS, 2, W, TC>(), TC>(prm, L, s);
   if (L.group <= 4) return launch_t<KV, D, BS, 4, stages_per_warp<KV, D, BS, 4, W, TC>(), TC>(prm, L, s);
   return launch_t<KV, D, BS, 8, stages_per_warp<KV, D, BS, 8, W, TC>(), TC>(prm, L, s);
@@ -2772,6 +2848,9 @@ cudaError_t launch_decode_kv(const PoolDev& pool, const PoolMaps& maps, const vo
   prm.n_cg = L.n_q > 1 ? L.n_cg : 1;
   prm.tpg = L.n_q > 1 ? L.tpg : 1;
   prm.g_heads = L.n_q > 1 ? L.g_heads : L.group;
+  prm.k_new = static_cast<const __nv_bfloat16*>(L.k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(L.v_new);
+  prm.append = (L.n_q <= 1 && L.k_new != nullptr && L.v_new != nullptr) ? 1 : 0;
   return dispatch_kv<KV>(prm, L, stream);
 }
 

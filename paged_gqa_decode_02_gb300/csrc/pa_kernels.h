@@ -31,6 +31,10 @@ struct DecodeLaunch {
   int n_cg;
   int tpg;
   int g_heads;
+  // fused decode step (n_q == 1): store each sequence's last token from
+  // k_new / v_new (bf16 [batch][Hkv][D]) before attending; null otherwise
+  const void* k_new;
+  const void* v_new;
   // workspace carve-up
   int32_t* pre_cost;    // [batch + 1] per-head cost-line prefix of the sequences
   float* part_o;        // [num_ctas + batch*Hkv][group][D]
