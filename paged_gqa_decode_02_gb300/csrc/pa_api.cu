@@ -88,11 +88,11 @@ struct DeviceGuard {
 // Default phantom pages per unit of the cost-balanced partition: the fixed
 // work of a unit (query load, state deposit and merge, row or partial write)
 // in page times of the pool's decode kernel, as measured on GB300 over the
-// Qwen-shaped bf16 and uint8 workloads and the prefix-sharing mix (uint8
-// pages are short to stream and costly to decode, so a unit weighs more;
-// fp8 pages, of the same size and decoded the same way, take uint8's value).
+// Qwen-shaped bf16, uint8 and fp8 workloads and the prefix-sharing mix
+// (quantised pages are short to stream and costly to decode, so a unit weighs
+// more: 10 for uint8, 14 for fp8, whose pages stream faster still).
 int32_t default_unit_cost(const pa_pool* p) {
-  return p->desc.kv_dtype == PA_KV_UINT8 || p->desc.kv_dtype == PA_KV_FP8 ? 10 : 6;
+  return p->desc.kv_dtype == PA_KV_UINT8 ? 10 : (p->desc.kv_dtype == PA_KV_FP8 ? 14 : 6);
 }
 
 bool uses_tensor_cores(const pa_pool* p) {
